@@ -1,0 +1,262 @@
+"""FastGen oracle: a plain float64 CPU statement of the adaptive KV-cache path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product imports this module; only
+the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline arm may
+call it.  It shares no code with the CUDA path.
+
+Sources (the FastGen paper, "Model Tells You What to Discard: Adaptive KV
+Cache Compression for LLMs", ICLR 2024, as summarised on the hyper.ai pages
+in Chinese and Korean/English; same text on both):
+  * Method, first paragraph: two phases.  Prompt encoding profiles every
+    attention head; generation keeps a head-specific KV cache to which new
+    keys/values are appended.
+  * Method, eq. (C*): C* = argmin_C CacheMemoryCost(C) subject to
+    |A - softmax(Q K_C^T)| <= 1 - T, with A = softmax(Q K^T).
+  * Method, base policies: C_special (special tokens such as the
+    begin-of-sequence marker), C_punct (punctuation), C_local (recent tokens
+    within a relative distance set by r_l), C_frequent (the tokens with the
+    largest cumulative attention scores, share r_f), C_full.
+  * Method, eq. for the shortlist: {special, special+punct,
+    special+punct+frequent, special+punct+frequent+local, full}, hybrids
+    being unions of base caches.
+  * Method, stability paragraph: the policy chosen at the prompt is reused
+    for all generated tokens.
+
+Readings of points the pages leave open (each is listed in the design notes):
+  R1 scores are scaled by s = 1/sqrt(d) unless a scale is given; the prompt
+     map is causal (row i sees keys j <= i).
+  R2 the distance in eq. (C*) is half the L1 norm per query row, averaged
+     uniformly over all n rows.  Renormalising A over a kept set K_i gives
+     (1/2)||A_i - Ahat_i||_1 = 1 - m_i with m_i the kept mass, so the
+     constraint is mean_i m_i >= T.
+  R3 w = ceil(r_l * n) and k = ceil(r_f * n), evaluated exactly on the
+     float32 value of the ratio.
+  R4 the local set of query row i is {j : i - w < j <= i}; the final cache of
+     a local-containing policy keeps the last w prompt positions.
+  R5 the frequent set is the top-k of colsum_j = sum_i A_ij over all prompt
+     keys, ties going to the lower index.
+  R6 policy = the cheapest shortlist entry whose mass is >= T; equal cost goes
+     to the earlier entry; the full cache has mass exactly 1.
+  R7 decoding: a new token is cached by a head iff its policy is full, or
+     its policy contains special and the token is special, or it contains
+     punct and the token is punctuation, or the policy contains local (the
+     token then lives in the window).  Special/punct/frequent members never
+     leave the cache; window members leave it once they are w positions old.
+     The frequent set is frozen at the prompt.  The query attends over the
+     cache after the new token is placed; an empty cache yields zeros.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# shortlist order of eq. (C*)'s policy set
+POLICIES = ("special", "special+punct", "special+punct+frequent",
+            "special+punct+frequent+local", "full")
+P_S, P_SP, P_SPF, P_SPFL, P_FULL = range(5)
+
+# cache-membership codes of the keep mask
+DROP, KEEP_STATIC, KEEP_WINDOW = 0, 1, 2
+
+
+def default_scale(d: int) -> float:
+    """R1: 1/sqrt(d), the scale of the Llama attention the workloads copy."""
+    return 1.0 / math.sqrt(d)
+
+
+def ratio_count(r: float, n: int) -> int:
+    """R3: ceil(r * n) on the float32 value of r (exact in float64)."""
+    r32 = float(np.float32(r))
+    return int(math.ceil(r32 * n))
+
+
+def attention_map(Q: np.ndarray, K: np.ndarray, scale: float) -> np.ndarray:
+    """A = softmax(s Q K^T) with the causal mask (Method, eq. (C*); R1)."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    n = Q.shape[0]
+    S = scale * (Q @ K.T)
+    S[np.triu_indices(n, 1)] = -np.inf
+    S = S - S.max(axis=1, keepdims=True)
+    E = np.exp(S)
+    return E / E.sum(axis=1, keepdims=True)
+
+
+def cumulative_scores(A: np.ndarray) -> np.ndarray:
+    """colsum_j = sum_i A_ij: the cumulative attention score of key j that
+    C_frequent ranks by (Method, base policies; R5)."""
+    return A.sum(axis=0)
+
+
+def token_sets(ids, special_ids, punct_ids):
+    """Boolean masks of C_special and C_punct members among positions."""
+    ids = np.asarray(ids)
+    return np.isin(ids, np.asarray(special_ids)), np.isin(ids, np.asarray(punct_ids))
+
+
+def frequent_set(colsum: np.ndarray, k: int) -> np.ndarray:
+    """C_frequent: the k keys of largest colsum, lower index first on ties (R5)."""
+    order = np.argsort(-colsum, kind="stable")
+    m = np.zeros(colsum.shape[0], dtype=bool)
+    m[order[:k]] = True
+    return m
+
+
+def local_rows(n: int, w: int) -> np.ndarray:
+    """C_local per query row i: {j : i - w < j <= i} (R4), as an [n, n] mask."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    return (j <= i) & (j > i - w)
+
+
+def candidate_row_masks(n, spec, punc, freq, w):
+    """Per-row kept sets K_i^p of the first four shortlist entries (unions of
+    base caches; Method, shortlist equation)."""
+    k0 = np.broadcast_to(spec, (n, n))
+    k1 = np.broadcast_to(spec | punc, (n, n))
+    k2 = np.broadcast_to(spec | punc | freq, (n, n))
+    k3 = k2 | local_rows(n, w)
+    return [k0, k1, k2, k3]
+
+
+def kept_mass(A: np.ndarray, row_mask: np.ndarray) -> float:
+    """mean_i sum_{j in K_i} A_ij, which is 1 - mean_i (1/2)||A_i - Ahat_i||_1 (R2)."""
+    n = A.shape[0]
+    return float((A * row_mask).sum() / n)
+
+
+def final_sets(n, spec, punc, freq, w):
+    """Positions kept at the end of the prompt by each shortlist entry, as
+    keep-code vectors (DROP / KEEP_STATIC / KEEP_WINDOW)."""
+    out = []
+    static = [spec, spec | punc, spec | punc | freq]
+    for s in static:
+        out.append(np.where(s, KEEP_STATIC, DROP).astype(np.uint8))
+    win = np.arange(n) >= n - w
+    k3 = np.where(static[2], KEEP_STATIC, np.where(win, KEEP_WINDOW, DROP)).astype(np.uint8)
+    out.append(k3)
+    out.append(np.full(n, KEEP_STATIC, dtype=np.uint8))
+    return out
+
+
+def choose_policy(mass, cost, T: float) -> int:
+    """eq. (C*): the cheapest entry with mass >= T; ties go to the earlier entry."""
+    feasible = [p for p in range(5) if mass[p] >= T]
+    return min(feasible, key=lambda p: (cost[p], p))
+
+
+def profile_head(Q, K, ids, special_ids, punct_ids, T, r_l, r_f, scale=None):
+    """Profile one head over its prompt (Method: prompt-encoding phase).
+
+    Q, K: [n, d] (any float dtype; upcast to float64).  ids: [n] token ids.
+    Returns dict(policy, mass[5], cost[5], colsum[n], keep[n] uint8, kept,
+    w, k, A).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    n, d = Q.shape
+    s = default_scale(d) if scale is None else scale
+    w, k = ratio_count(r_l, n), ratio_count(r_f, n)
+    A = attention_map(Q, K, s)
+    colsum = cumulative_scores(A)
+    spec, punc = token_sets(ids[:n], special_ids, punct_ids)
+    freq = frequent_set(colsum, k)
+    masks = candidate_row_masks(n, spec, punc, freq, w)
+    mass = [kept_mass(A, m) for m in masks] + [1.0]
+    finals = final_sets(n, spec, punc, freq, w)
+    cost = [int((f != DROP).sum()) for f in finals]
+    p = choose_policy(mass, cost, T)
+    return dict(policy=p, mass=np.array(mass), cost=np.array(cost),
+                colsum=colsum, keep=finals[p], kept=cost[p], w=w, k=k, A=A,
+                freq=freq)
+
+
+def masses_from_column_scores(colsum, bandcol, spec, punc, freq):
+    """Column form of the four candidate masses (exact algebra on eq. (C*)'s
+    per-row sums): for p <= 2 the kept mass is sum_{j in K^p} colsum_j / n;
+    for the local hybrid it is [sum_j bandcol_j + sum_{j in K^2}
+    (colsum_j - bandcol_j)] / n, with bandcol_j = sum_{i=j}^{j+w-1} A_ij.
+    Used to cross-check the per-row definition."""
+    n = colsum.shape[0]
+    k2 = spec | punc | freq
+    m0 = colsum[spec].sum() / n
+    m1 = colsum[spec | punc].sum() / n
+    m2 = colsum[k2].sum() / n
+    m3 = (bandcol.sum() + (colsum[k2] - bandcol[k2]).sum()) / n
+    return np.array([m0, m1, m2, m3, 1.0])
+
+
+def band_scores(A: np.ndarray, w: int) -> np.ndarray:
+    """bandcol_j = sum_{i=j}^{min(j+w-1, n-1)} A_ij."""
+    n = A.shape[0]
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    band = (i >= j) & (i < j + w)
+    return (A * band).sum(axis=0)
+
+
+def compact_head(K, V, keep):
+    """K_C, V_C = f(K, V, C) (Method, second paragraph): the kept prompt
+    rows in position order, split into never-evicted members and window
+    members.  Returns (static_pos, window_pos, K_static, V_static, K_win, V_win)."""
+    keep = np.asarray(keep)
+    sp = np.nonzero(keep == KEEP_STATIC)[0]
+    wp = np.nonzero(keep == KEEP_WINDOW)[0]
+    K = np.asarray(K)
+    V = np.asarray(V)
+    return sp, wp, K[sp], V[sp], K[wp], V[wp]
+
+
+def stores_static(policy: int, is_special: bool, is_punct: bool) -> bool:
+    """R7: does a generated token join the never-evicted part of the cache?"""
+    if policy == P_FULL:
+        return True
+    if policy == P_S:
+        return is_special
+    return is_special or is_punct
+
+
+def attend(q, Kc, Vc, scale):
+    """Single-query attention softmax(s q K_c^T) V_c over a cache (zeros if empty)."""
+    q = np.asarray(q, dtype=np.float64)
+    if Kc.shape[0] == 0:
+        return np.zeros(q.shape[0])
+    s = scale * (np.asarray(Kc, dtype=np.float64) @ q)
+    e = np.exp(s - s.max())
+    return (e / e.sum()) @ np.asarray(Vc, dtype=np.float64)
+
+
+def decode_positions(policy, static_pos, w, t):
+    """Cache positions seen by the query at position t (after placement):
+    the never-evicted members plus, for the local hybrid, the window
+    (t - w, t] (R7)."""
+    pos = set(int(p) for p in static_pos)
+    if policy == P_SPFL:
+        pos.update(range(max(t - w + 1, 0), t + 1))
+    return np.array(sorted(pos), dtype=np.int64)
+
+
+def decode_head(policy, keep, n, w, ids, Qall, Kall, Vall, special_ids, punct_ids,
+                steps, scale=None):
+    """Token generation with the head-specific cache (Method, first and
+    stability paragraphs): for t = n .. n+steps-1, place token t by R7 and
+    attend with q_t.  Qall/Kall/Vall: [n + steps, d]; ids: [n + steps].
+    Returns (out [steps, d], final cache positions)."""
+    Kall = np.asarray(Kall, dtype=np.float64)
+    Vall = np.asarray(Vall, dtype=np.float64)
+    Qall = np.asarray(Qall, dtype=np.float64)
+    d = Kall.shape[1]
+    s = default_scale(d) if scale is None else scale
+    sset, pset = set(int(x) for x in special_ids), set(int(x) for x in punct_ids)
+    static = [int(j) for j in np.nonzero(np.asarray(keep) == KEEP_STATIC)[0]]
+    out = np.zeros((steps, d))
+    pos = np.array(static, dtype=np.int64)
+    for step in range(steps):
+        t = n + step
+        tau = int(ids[t])
+        if stores_static(policy, tau in sset, tau in pset):
+            static.append(t)
+        pos = decode_positions(policy, static, w, t)
+        out[step] = attend(Qall[t], Kall[pos], Vall[pos], s)
+    return out, pos

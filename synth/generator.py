@@ -1,0 +1,258 @@
+"""Counter-based generator of the synthetic FastGen workloads.
+
+The FastGen pages measure on Llama 1 models with real prompts; neither the
+weights nor the datasets are available here, so these seeded inputs stand in
+for them, with the attention shapes of the Llama configurations and the head
+types the pages describe (special-token heads, punctuation heads, local heads
+and broad heads: jisaku.com "FastGen" glossary, section on the four head
+types; hyper.ai ICLR 2024 summary, Method, the paragraph on head behaviour).
+
+Every value is a pure function of (seed, stream, indices): a splitmix64 hash
+(Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+OOPSLA 2014) of a 64-bit counter gives uniforms, and the Box-Muller transform
+(Box and Muller, 1958) in float64 turns pairs of uniforms into normals. A head
+can therefore be regenerated alone, on any machine, without generating the
+others. Tensors are rounded once, to the working dtype, after the float64
+values are formed.
+
+Planted structure per head type (per layer-head (l, h); noise per (b, l, h)):
+  special : u ~ N(0, I_d); K_j += 4u at special-token positions, Q_i += 4u.
+  punct   : v ~ N(0, I_d); K_j += 4v at punctuation positions, Q_i += 4v.
+  local   : Q_i = RoPE_i(c) + N(0, I), K_j = RoPE_j(c) + N(0, I), c = 3z,
+            z ~ N(0, I_d), RoPE base 10000 on interleaved pairs.
+  broad   : Q, K ~ N(0, I).
+V ~ N(0, I) for every head.  Positions 0..n-1 are the prompt; positions
+n..n+steps-1 are the tokens fed one by one during decoding.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+
+HEAD_TYPES = ("special", "punct", "local", "broad")
+VOCAB = 32000
+BOS_ID = 1
+PUNCT_FRACTION = 0.05
+N_PUNCT_IDS = 10
+
+_M64 = (1 << 64) - 1
+_GAMMA = 0x9E3779B97F4A7C15
+_MIX1 = 0xBF58476D1CE4E5B9
+_MIX2 = 0x94D049BB133111EB
+
+# stream tags, one per independent draw
+_S_IDS, _S_PUNCT_DRAW, _S_PUNCT_SET, _S_TYPE = 1, 2, 3, 4
+_S_PLANT, _S_Q, _S_K, _S_V = 5, 6, 7, 8
+
+
+def _mix_scalar(x: int) -> int:
+    z = (x + _GAMMA) & _M64
+    z = ((z ^ (z >> 30)) * _MIX1) & _M64
+    z = ((z ^ (z >> 27)) * _MIX2) & _M64
+    return z ^ (z >> 31)
+
+
+def _key(*parts: int) -> int:
+    h = 0
+    for p in parts:
+        h = _mix_scalar(h ^ (int(p) & _M64))
+    return h
+
+
+def _mix_vec(x: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = x + np.uint64(_GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(_MIX1)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(_MIX2)
+        return z ^ (z >> np.uint64(31))
+
+
+def _bits(key: int, count: int) -> np.ndarray:
+    ctr = np.arange(count, dtype=np.uint64) + np.uint64(key)
+    return _mix_vec(ctr)
+
+
+def _uniform(key: int, count: int) -> np.ndarray:
+    """Uniforms in [0, 1) with 53 random bits."""
+    return (_bits(key, count) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+
+
+def _normal(key: int, count: int) -> np.ndarray:
+    """Standard normals by Box-Muller from counter-indexed uniform pairs."""
+    pairs = (count + 1) // 2
+    b = _bits(key, 2 * pairs)
+    u1 = ((b[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53  # (0, 1]
+    u2 = (b[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = 2.0 * math.pi * u2
+    out = np.empty(2 * pairs, dtype=np.float64)
+    out[0::2] = r * np.cos(t)
+    out[1::2] = r * np.sin(t)
+    return out[:count]
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    B: int
+    L: int
+    H: int
+    d: int
+    n: int
+    steps: int
+    dtype: str  # "bf16" or "fp32"
+    T: float
+    r_l: float
+    r_f: float
+    mix: tuple = (0.15, 0.20, 0.35, 0.30)  # special / punct / local / broad
+    one_of_each: bool = False  # tiny: head h of each layer has type h % 4
+    extra: dict = field(default_factory=dict, compare=False)
+
+    @property
+    def G(self) -> int:
+        return self.B * self.L * self.H
+
+    def with_(self, **kw) -> "Config":
+        return replace(self, **kw)
+
+
+_LONG_MIX = (0.15 * 0.6 / 0.7, 0.20 * 0.6 / 0.7, 0.35 * 0.6 / 0.7, 0.40)
+
+CONFIGS = {
+    "tiny": Config("tiny", 1, 1, 4, 64, 128, 16, "fp32", 0.95, 0.3, 0.3, one_of_each=True),
+    "llama7b": Config("llama7b", 1, 32, 32, 128, 2048, 256, "bf16", 0.95, 0.3, 0.3),
+    "llama13b": Config("llama13b", 4, 40, 40, 128, 4096, 512, "bf16", 0.95, 0.3, 0.3),
+    "llama65b": Config("llama65b", 8, 80, 64, 128, 2048, 1024, "bf16", 0.95, 0.3, 0.3),
+    "long8k": Config("long8k", 1, 32, 32, 128, 8192, 256, "bf16", 0.95, 0.1, 0.2, _LONG_MIX),
+    "long16k": Config("long16k", 1, 32, 32, 128, 16384, 256, "bf16", 0.95, 0.1, 0.2, _LONG_MIX),
+    "long32k": Config("long32k", 1, 32, 32, 128, 32768, 256, "bf16", 0.95, 0.1, 0.2, _LONG_MIX),
+}
+
+
+def special_ids(seed: int = 0) -> np.ndarray:
+    """The special-token id set: the begin-of-sequence marker alone."""
+    return np.array([BOS_ID], dtype=np.int32)
+
+
+def punct_ids(seed: int = 0) -> np.ndarray:
+    """Ten distinct stand-in punctuation ids, drawn once from [3, VOCAB)."""
+    out: list[int] = []
+    i = 0
+    while len(out) < N_PUNCT_IDS:
+        v = 3 + int(_mix_scalar(_key(seed, _S_PUNCT_SET, i)) % (VOCAB - 3))
+        if v not in out:
+            out.append(v)
+        i += 1
+    return np.array(out, dtype=np.int32)
+
+
+def make_ids(cfg: Config, seed: int = 0) -> np.ndarray:
+    """Token ids [B, n + steps]: uniform over the vocabulary, BOS at 0, and
+    about 5 % of positions replaced by an id from the punctuation set."""
+    total = cfg.n + cfg.steps
+    pset = punct_ids(seed)
+    ids = np.empty((cfg.B, total), dtype=np.int32)
+    for b in range(cfg.B):
+        u = _bits(_key(seed, _S_IDS, b), total)
+        row = (u % np.uint64(VOCAB)).astype(np.int64)
+        pick = _uniform(_key(seed, _S_PUNCT_DRAW, b), 2 * total)
+        is_p = pick[0::2] < PUNCT_FRACTION
+        which = np.minimum((pick[1::2] * len(pset)).astype(np.int64), len(pset) - 1)
+        row = np.where(is_p, pset[which], row)
+        row[0] = BOS_ID
+        ids[b] = row.astype(np.int32)
+    return ids
+
+
+def head_types(cfg: Config, seed: int = 0) -> np.ndarray:
+    """Head type per (layer, head) as an index into HEAD_TYPES."""
+    t = np.empty((cfg.L, cfg.H), dtype=np.int32)
+    cum = np.cumsum(np.asarray(cfg.mix, dtype=np.float64))
+    for l in range(cfg.L):
+        for h in range(cfg.H):
+            if cfg.one_of_each:
+                t[l, h] = h % 4
+            else:
+                u = _uniform(_key(seed, _S_TYPE, l, h), 1)[0]
+                t[l, h] = int(min(np.searchsorted(cum, u, side="right"), 3))
+    return t
+
+
+def _rope(c: np.ndarray, positions: np.ndarray, base: float = 10000.0) -> np.ndarray:
+    d = c.shape[0]
+    k = np.arange(d // 2, dtype=np.float64)
+    theta = base ** (-2.0 * k / d)
+    ang = positions[:, None].astype(np.float64) * theta[None, :]
+    cs, sn = np.cos(ang), np.sin(ang)
+    x, y = c[0::2][None, :], c[1::2][None, :]
+    out = np.empty((positions.shape[0], d), dtype=np.float64)
+    out[:, 0::2] = x * cs - y * sn
+    out[:, 1::2] = x * sn + y * cs
+    return out
+
+
+def make_head(cfg: Config, seed: int, g: int, ids: np.ndarray, types: np.ndarray):
+    """float64 (Q, K, V), each [n + steps, d], of head instance g = (b*L + l)*H + h."""
+    b, rem = divmod(g, cfg.L * cfg.H)
+    l, h = divmod(rem, cfg.H)
+    total, d = cfg.n + cfg.steps, cfg.d
+    kind = HEAD_TYPES[types[l, h]]
+    Q = _normal(_key(seed, _S_Q, b, l, h), total * d).reshape(total, d)
+    K = _normal(_key(seed, _S_K, b, l, h), total * d).reshape(total, d)
+    V = _normal(_key(seed, _S_V, b, l, h), total * d).reshape(total, d)
+    plant = _normal(_key(seed, _S_PLANT, l, h), d)
+    if kind == "special":
+        mask = np.isin(ids[b], special_ids(seed))
+        K[mask] += 4.0 * plant
+        Q += 4.0 * plant
+    elif kind == "punct":
+        mask = np.isin(ids[b], punct_ids(seed))
+        K[mask] += 4.0 * plant
+        Q += 4.0 * plant
+    elif kind == "local":
+        r = _rope(3.0 * plant, np.arange(total))
+        Q += r
+        K += r
+    return Q, K, V
+
+
+def _round(x: np.ndarray, dtype: str):
+    import torch
+
+    t = torch.from_numpy(x)
+    return t.to(torch.bfloat16) if dtype == "bf16" else t.to(torch.float32)
+
+
+def make_workload(cfg: Config, seed: int = 0, heads=None, threads: int | None = None):
+    """Rounded CPU tensors for a whole workload (or a subset of head indices).
+
+    Returns dict(Q, K, V: [len(heads), n + steps, d] in the working dtype,
+    ids: [B, n + steps] int32, types: [L, H], heads: the head indices).
+    """
+    import torch
+
+    heads = np.arange(cfg.G) if heads is None else np.asarray(heads, dtype=np.int64)
+    ids = make_ids(cfg, seed)
+    types = head_types(cfg, seed)
+    total = cfg.n + cfg.steps
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    out = {k: torch.empty((len(heads), total, cfg.d), dtype=tdt) for k in "QKV"}
+
+    def one(i):
+        q, k, v = make_head(cfg, seed, int(heads[i]), ids, types)
+        out["Q"][i] = _round(q, cfg.dtype)
+        out["K"][i] = _round(k, cfg.dtype)
+        out["V"][i] = _round(v, cfg.dtype)
+
+    nthr = threads or min(32, os.cpu_count() or 1)
+    if nthr <= 1 or len(heads) <= 1:
+        for i in range(len(heads)):
+            one(i)
+    else:
+        with ThreadPoolExecutor(nthr) as ex:
+            list(ex.map(one, range(len(heads))))
+    return dict(out, ids=ids, types=types, heads=heads)
