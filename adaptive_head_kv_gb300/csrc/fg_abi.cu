@@ -1,0 +1,240 @@
+// C ABI of the FastGen hot path: argument checks, workspace carving and the
+// launch sequence of each call.  All memory belongs to the caller.
+#include <math.h>
+#include <stdint.h>
+
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace {
+
+using fg::cdiv;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxIdSet = 4096;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int ratio_count(float r, int n) { return (int)ceil((double)r * (double)n); }
+
+fg_status check_params(const fg_params* p) {
+  if (!p) return FG_EINVAL;
+  if (p->B < 1 || p->L < 1 || p->H < 1 || p->n < 1) return FG_EINVAL;
+  const long long G = (long long)p->B * p->L * p->H;
+  if (G > 0x7fffffffLL || (long long)G * p->n > (1LL << 40)) return FG_EINVAL;
+  if (p->d != 64 && p->d != 128) return FG_EDTYPE;
+  if (p->dtype != FG_BF16 && p->dtype != FG_FP32) return FG_EDTYPE;
+  if (!(p->T > 0.f && p->T <= 1.f)) return FG_EINVAL;
+  if (!(p->r_l >= 0.f && p->r_l <= 1.f) || !(p->r_f >= 0.f && p->r_f <= 1.f)) return FG_EINVAL;
+  if (!(p->scale >= 0.f) || isinf(p->scale)) return FG_EINVAL;
+  return FG_OK;
+}
+
+fg::ProfileDims dims(const fg_params* p) {
+  fg::ProfileDims pd;
+  pd.B = p->B;
+  pd.HL = p->L * p->H;
+  pd.G = p->B * pd.HL;
+  pd.n = p->n;
+  pd.d = p->d;
+  pd.dtype = p->dtype;
+  pd.w = ratio_count(p->r_l, p->n);
+  pd.k = ratio_count(p->r_f, p->n);
+  pd.T = p->T;
+  const float s = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)p->d));
+  pd.sl2 = s * fg::kLog2e;
+  return pd;
+}
+
+fg_status check_ids(const int32_t* set, int32_t cnt) {
+  if (cnt < 0 || cnt > kMaxIdSet) return FG_EINVAL;
+  if (cnt > 0 && !set) return FG_EINVAL;
+  return FG_OK;
+}
+
+fg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FG_OK : FG_ECUDA; }
+
+size_t elem_bytes(const fg_params* p) { return p->dtype == FG_BF16 ? 2 : 4; }
+
+// plan buffer: [G descriptors][2 x int64 totals][work list]
+size_t plan_desc_bytes(int G) { return align_up((size_t)G * sizeof(fg_head_desc)); }
+size_t plan_max_work(const fg_params* p, int32_t max_new) {
+  const size_t G = (size_t)p->B * p->L * p->H;
+  const int w = ratio_count(p->r_l, p->n);
+  return G * (size_t)(cdiv(p->n + max_new, fg::kRowsPerWork) + cdiv(w, fg::kRowsPerWork));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fastgen_status_string(fg_status s) {
+  switch (s) {
+    case FG_OK: return "ok";
+    case FG_EINVAL: return "invalid argument";
+    case FG_EDTYPE: return "unsupported dtype or head dim";
+    case FG_EWORKSPACE: return "workspace, plan or pool buffer too small";
+    case FG_ECAPACITY: return "a head ran out of reserved cache rows";
+    case FG_ECUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int32_t fastgen_version(void) { return 100; }
+
+size_t fastgen_profile_workspace_bytes(const fg_params* p) {
+  if (check_params(p) != FG_OK) return 0;
+  const size_t G = (size_t)p->B * p->L * p->H, n = p->n;
+  return 2 * align_up(G * n * sizeof(float)) + align_up((size_t)p->B * n);
+}
+
+fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
+                          const int32_t* token_ids, const int32_t* special_ids,
+                          int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                          int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                          uint8_t* keep, int32_t* kept, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
+  if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
+  if (!Q || !K || !token_ids || !policy || !mass || !cost || !colsum || !keep || !kept ||
+      !workspace)
+    return FG_EINVAL;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(workspace, kAlign) || !aligned(mass, 4) ||
+      !aligned(cost, 4) || !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4))
+    return FG_EINVAL;
+  if (workspace_bytes < fastgen_profile_workspace_bytes(p)) return FG_EWORKSPACE;
+  const fg::ProfileDims pd = dims(p);
+  const size_t Gn = (size_t)pd.G * pd.n;
+  char* ws = (char*)workspace;
+  float* lse2 = (float*)ws;
+  float* bandcol = (float*)(ws + align_up(Gn * sizeof(float)));
+  uint8_t* cls = (uint8_t*)(ws + 2 * align_up(Gn * sizeof(float)));
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
+                                         punct_ids, n_punct, cls, s);
+  if (e == cudaSuccess) e = fg::launch_profile_simt(pd, Q, K, lse2, colsum, bandcol, s);
+  if (e == cudaSuccess)
+    e = fg::launch_select(pd, colsum, bandcol, cls, policy, mass, cost, keep, kept, s);
+  return cuda_status(e);
+}
+
+size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens) {
+  if (check_params(p) != FG_OK || max_new_tokens < 0) return 0;
+  const int G = p->B * p->L * p->H;
+  return plan_desc_bytes(G) + kAlign + plan_max_work(p, max_new_tokens) * sizeof(int2);
+}
+
+fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const int32_t* cost,
+                               int32_t max_new_tokens, void* plan, size_t plan_bytes,
+                               fg_plan_info* info, void* stream) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if (!policy || !cost || !plan || !info || max_new_tokens < 0) return FG_EINVAL;
+  if (!aligned(plan, kAlign) || !aligned(cost, 4)) return FG_EINVAL;
+  if ((long long)p->n + max_new_tokens > 0x7fffffffLL - fg::kRowsPerWork) return FG_EINVAL;
+  if (plan_bytes < fastgen_plan_bytes(p, max_new_tokens)) return FG_EWORKSPACE;
+  const fg::ProfileDims pd = dims(p);
+  char* base = (char*)plan;
+  fg_head_desc* desc = (fg_head_desc*)base;
+  long long* totals = (long long*)(base + plan_desc_bytes(pd.G));
+  int2* work = (int2*)(base + plan_desc_bytes(pd.G) + kAlign);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = fg::launch_plan(pd.G, pd.w, max_new_tokens, policy, cost, desc, work, totals, s);
+  long long h[2] = {0, 0};
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h, totals, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return FG_ECUDA;
+  if (h[1] > (long long)plan_max_work(p, max_new_tokens) || h[1] > 0x7fffffffLL) return FG_ECUDA;
+  info->pool_rows = h[0];
+  info->n_work = (int32_t)h[1];
+  info->rows_per_work = fg::kRowsPerWork;
+  return FG_OK;
+}
+
+fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, const uint8_t* keep,
+                          const void* plan, const fg_plan_info* info, void* K_pool,
+                          void* V_pool, int32_t* pos_pool, int64_t pool_rows, void* stream) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if (!K || !V || !keep || !plan || !info || !K_pool || !V_pool || !pos_pool) return FG_EINVAL;
+  if (!aligned(K, 16) || !aligned(V, 16) || !aligned(K_pool, 16) || !aligned(V_pool, 16) ||
+      !aligned(plan, kAlign) || !aligned(pos_pool, 4))
+    return FG_EINVAL;
+  if (pool_rows < info->pool_rows) return FG_EWORKSPACE;
+  const fg::ProfileDims pd = dims(p);
+  cudaError_t e = fg::launch_compact(pd, K, V, keep, (const fg_head_desc*)plan, K_pool, V_pool,
+                                     pos_pool, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+size_t fastgen_decode_workspace_bytes(const fg_params* p, const fg_plan_info* info) {
+  if (check_params(p) != FG_OK || !info || info->n_work < 0) return 0;
+  const size_t nw = (size_t)info->n_work;
+  return align_up(nw * 2 * sizeof(float)) + align_up(nw * p->d * sizeof(float));
+}
+
+fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info* info,
+                              void* K_pool, void* V_pool, int32_t* pos_pool, const void* q,
+                              const void* k_new, const void* v_new, const int32_t* new_ids,
+                              const int32_t* special_ids, int32_t n_special,
+                              const int32_t* punct_ids, int32_t n_punct, int32_t pos,
+                              void* out, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, void* stream) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
+  if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
+  if (!plan || !info || !K_pool || !V_pool || !pos_pool || !q || !k_new || !v_new ||
+      !new_ids || !out || !workspace || !dev_err)
+    return FG_EINVAL;
+  if (!aligned(plan, kAlign) || !aligned(K_pool, 16) || !aligned(V_pool, 16) ||
+      !aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+      !aligned(workspace, kAlign) || !aligned(dev_err, 4) || !aligned(pos_pool, 4))
+    return FG_EINVAL;
+  if (pos < p->n || info->n_work < 0) return FG_EINVAL;
+  if (workspace_bytes < fastgen_decode_workspace_bytes(p, info)) return FG_EWORKSPACE;
+  const fg::ProfileDims pd = dims(p);
+  char* base = (char*)plan;
+  fg::DecodeArgs a;
+  a.desc = (fg_head_desc*)base;
+  a.work = (const int2*)(base + plan_desc_bytes(pd.G) + kAlign);
+  a.n_work = info->n_work;
+  a.Kp = K_pool;
+  a.Vp = V_pool;
+  a.posp = pos_pool;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_ids = new_ids;
+  a.special = special_ids;
+  a.ns = n_special;
+  a.punct = punct_ids;
+  a.np = n_punct;
+  a.pos = pos;
+  a.out = out;
+  char* ws = (char*)workspace;
+  a.part_ml = (float*)ws;
+  a.part_acc = (float*)(ws + align_up((size_t)info->n_work * 2 * sizeof(float)));
+  a.dev_err = dev_err;
+  if (info->n_work == 0) {
+    cudaError_t e = cudaMemsetAsync(out, 0, (size_t)pd.G * pd.d * elem_bytes(p),
+                                    (cudaStream_t)stream);
+    return cuda_status(e);
+  }
+  return cuda_status(fg::launch_decode(pd, a, (cudaStream_t)stream));
+}
+
+fg_status fastgen_read_error(const int32_t* dev_err, void* stream) {
+  if (!dev_err) return FG_EINVAL;
+  int32_t h = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&h, dev_err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FG_ECUDA;
+  return (h & 1) ? FG_ECAPACITY : FG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// Compaction: K_C, V_C = f(K, V, C) (Model Tells You What to Discard,
+// Method, second paragraph) into one pooled, ragged, per-head layout.
+//
+// Pool layout of head g (rows of d elements, K and V pools share it):
+//   [off, off + static_cap)        never-evicted segment: the kept static
+//                                  prompt rows in position order, then room
+//                                  for max_new_tokens appended rows;
+//   [win_off, win_off + w)         SPFL heads only: the window ring, the row
+//                                  of position t at slot t mod w.
+// The plan kernel lays heads out by an exclusive scan of their row counts
+// and also emits the decode work list (one item per kRowsPerWork rows).
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace fg {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kCompactThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
+    const int8_t* __restrict__ policy, const int32_t* __restrict__ cost, int G, int w,
+    int reserve, fg_head_desc* __restrict__ desc, long long* __restrict__ totals) {
+  __shared__ long long scr64[33];
+  __shared__ int scr32[33];
+  long long row_base = 0;
+  int work_base = 0;
+  for (int base = 0; base < G; base += blockDim.x) {
+    const int g = base + threadIdx.x;
+    long long rows = 0;
+    int works = 0, p = 0, n_static = 0, cap = 0, wg = 0;
+    if (g < G) {
+      p = policy[g];
+      n_static = (p == FG_POLICY_SPFL) ? cost[(size_t)g * 5 + 2] : cost[(size_t)g * 5 + p];
+      cap = n_static + reserve;
+      wg = (p == FG_POLICY_SPFL) ? w : 0;
+      rows = (long long)cap + wg;
+      works = cdiv(cap, kRowsPerWork) + cdiv(wg, kRowsPerWork);
+    }
+    long long rtot;
+    int wtot;
+    const long long roff = row_base + block_exclusive_scan(rows, scr64, &rtot);
+    const int woff = work_base + block_exclusive_scan(works, scr32, &wtot);
+    if (g < G) {
+      fg_head_desc hd;
+      hd.off = roff;
+      hd.n_static = n_static;
+      hd.static_cap = cap;
+      hd.win_off = roff + cap;
+      hd.w = wg;
+      hd.policy = p;
+      hd.work_off = woff;
+      hd.n_work = works;
+      desc[g] = hd;
+    }
+    row_base += rtot;
+    work_base += wtot;
+  }
+  if (threadIdx.x == 0) {
+    totals[0] = row_base;
+    totals[1] = work_base;
+  }
+}
+
+__global__ void worklist_kernel(const fg_head_desc* __restrict__ desc, int G,
+                                int2* __restrict__ work) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  const fg_head_desc hd = desc[g];
+  for (int i = 0; i < hd.n_work; ++i) work[hd.work_off + i] = make_int2(g, i);
+}
+
+// One CTA per head: scan the keep codes in tiles of 256 positions, then copy
+// the tile's kept rows with 16-byte vectors, one row per LPR lanes.
+template <typename T, int D>
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(
+    const T* __restrict__ K, const T* __restrict__ V, const uint8_t* __restrict__ keep,
+    const fg_head_desc* __restrict__ desc, int n, T* __restrict__ Kp, T* __restrict__ Vp,
+    int32_t* __restrict__ posp) {
+  constexpr int E = Vec16<T>::kElems;
+  constexpr int LPR = D / E;  // 16-byte vectors per row
+  __shared__ int scr[33];
+  __shared__ int src_pos[kCompactThreads];
+  __shared__ long long dst_row[kCompactThreads];
+  const int g = blockIdx.x;
+  const fg_head_desc hd = desc[g];
+  const uint8_t* kg = keep + (size_t)g * n;
+  // empty markers: reserve rows of the static segment and every ring slot
+  for (int r = hd.n_static + threadIdx.x; r < hd.static_cap; r += blockDim.x)
+    posp[hd.off + r] = -1;
+  for (int r = threadIdx.x; r < hd.w; r += blockDim.x) posp[hd.win_off + r] = -1;
+  __syncthreads();
+  int static_seen = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    const int code = j < n ? kg[j] : FG_KEEP_DROP;
+    const int is_static = code == FG_KEEP_STATIC;
+    const int is_kept = code != FG_KEEP_DROP;
+    int st_total, kept_total;
+    const int st_rank = static_seen + block_exclusive_scan(is_static, scr, &st_total);
+    const int slot = block_exclusive_scan(is_kept, scr, &kept_total);
+    if (is_kept) {
+      long long dst;
+      if (is_static) dst = hd.off + st_rank;
+      else dst = hd.win_off + (hd.w > 0 ? j % hd.w : 0);
+      posp[dst] = j;
+      src_pos[slot] = j;
+      dst_row[slot] = dst;
+    }
+    static_seen += st_total;
+    __syncthreads();
+    const T* Kg = K + (size_t)g * n * D;
+    const T* Vg = V + (size_t)g * n * D;
+    for (int v = threadIdx.x; v < kept_total * LPR; v += blockDim.x) {
+      const int r = v / LPR, c = (v % LPR) * E;
+      const size_t s = (size_t)src_pos[r] * D + c;
+      const size_t d = (size_t)dst_row[r] * D + c;
+      const uint4 kv = ldg_stream(Kg + s);
+      const uint4 vv = ldg_stream(Vg + s);
+      *reinterpret_cast<uint4*>(Kp + d) = kv;
+      *reinterpret_cast<uint4*>(Vp + d) = vv;
+    }
+    __syncthreads();
+  }
+}
+
+template <typename T, int D>
+cudaError_t run_compact(const ProfileDims& pd, const void* K, const void* V, const uint8_t* keep,
+                        const fg_head_desc* desc, void* Kp, void* Vp, int32_t* posp,
+                        cudaStream_t s) {
+  compact_kernel<T, D><<<pd.G, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
+                                                        pd.n, (T*)Kp, (T*)Vp, posp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plan(int G, int w, int reserve, const int8_t* policy, const int32_t* cost,
+                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(policy, cost, G, w, reserve, desc, totals);
+  worklist_kernel<<<cdiv(G, 256), 256, 0, s>>>(desc, G, work);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const ProfileDims& pd, const void* K, const void* V,
+                           const uint8_t* keep, const fg_head_desc* desc, void* Kp, void* Vp,
+                           int32_t* posp, cudaStream_t s) {
+  if (pd.dtype == FG_FP32)
+    return pd.d == 64 ? run_compact<float, 64>(pd, K, V, keep, desc, Kp, Vp, posp, s)
+                      : run_compact<float, 128>(pd, K, V, keep, desc, Kp, Vp, posp, s);
+  return pd.d == 64 ? run_compact<__nv_bfloat16, 64>(pd, K, V, keep, desc, Kp, Vp, posp, s)
+                    : run_compact<__nv_bfloat16, 128>(pd, K, V, keep, desc, Kp, Vp, posp, s);
+}
+
+}  // namespace fg

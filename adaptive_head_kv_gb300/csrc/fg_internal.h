@@ -1,0 +1,65 @@
+// Launchers shared between the C-ABI translation unit and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fastgen.h"
+
+namespace fg {
+
+// Decode work item: up to kRowsPerWork consecutive cache rows of one head.
+constexpr int kRowsPerWork = 256;
+
+struct ProfileDims {
+  int G, HL, B, n, d, dtype;
+  int w, k;
+  float T, sl2;  // sl2 = scale * log2(e): scores are kept in base-2 units
+};
+
+// Token class per prompt position: bit 0 special, bit 1 punctuation.
+cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
+                               const int32_t* punct, int np, uint8_t* cls, cudaStream_t s);
+
+// Pass 1 (row log-sum-exp, base 2) and pass 2 (column and band sums), plain
+// SIMT fp32 arithmetic.
+cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
+                                float* colsum, float* bandcol, cudaStream_t s);
+
+// Top-k frequent set, candidate masses, policy, keep codes.
+cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,
+                          const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
+                          uint8_t* keep, int32_t* kept, cudaStream_t s);
+
+cudaError_t launch_plan(int G, int w, int reserve, const int8_t* policy, const int32_t* cost,
+                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s);
+
+cudaError_t launch_compact(const ProfileDims& pd, const void* K, const void* V,
+                           const uint8_t* keep, const fg_head_desc* desc, void* Kp, void* Vp,
+                           int32_t* posp, cudaStream_t s);
+
+struct DecodeArgs {
+  fg_head_desc* desc;
+  const int2* work;
+  int n_work;
+  void* Kp;
+  void* Vp;
+  int32_t* posp;
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* new_ids;
+  const int32_t* special;
+  int ns;
+  const int32_t* punct;
+  int np;
+  int pos;
+  void* out;
+  float* part_ml;   // [n_work, 2]
+  float* part_acc;  // [n_work, d]
+  int32_t* dev_err;
+};
+
+cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace fg

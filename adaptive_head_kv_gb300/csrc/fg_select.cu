@@ -1,0 +1,183 @@
+// Policy selection per head (Model Tells You What to Discard, Method:
+// base policies, shortlist and eq. (C*)).
+//
+// One CTA per head.  From the column sums of the attention map it
+//   1. picks C_frequent = the k keys of largest colsum (ties to the lower
+//      index) by an MSB-first radix select on the fp32 bit patterns (colsum
+//      >= 0, so unsigned order is value order);
+//   2. forms the four candidate masses from column sums alone:
+//        mass_p = sum_{j in K^p} colsum_j / n                    (p <= 2)
+//        mass_3 = [sum_j bandcol_j + sum_{j in K^2} (colsum_j - bandcol_j)] / n
+//      which equals the per-row mean of the kept attention (the local set of
+//      row i, {i-w < j <= i}, contributes band sums column by column);
+//   3. takes the first shortlist entry with mass >= T (the cheapest, as the
+//      entries are nested) and writes the keep codes of its final cache.
+#include "fg_common.cuh"
+#include "fg_internal.h"
+
+namespace fg {
+namespace {
+
+constexpr int kSelThreads = 512;
+
+__global__ void token_class_kernel(const int32_t* __restrict__ ids, int count,
+                                   const int32_t* __restrict__ special, int ns,
+                                   const int32_t* __restrict__ punct, int np,
+                                   uint8_t* __restrict__ cls) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const int id = ids[i];
+  cls[i] = (uint8_t)((id_in(id, special, ns) ? 1 : 0) | (id_in(id, punct, np) ? 2 : 0));
+}
+
+template <typename V>
+__device__ __forceinline__ V block_sum(V x, V* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  V t = V(0);
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+  return t;
+}
+
+// Membership bits kept in `keep` between the two sweeps: 1 = K^0,
+// 2 = K^1, 4 = K^2, 8 = inside the last-w window.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(
+    const float* __restrict__ colsum, const float* __restrict__ bandcol,
+    const uint8_t* __restrict__ cls, int n, int HL, int k, int w, float T,
+    int8_t* __restrict__ policy, float* __restrict__ mass, int32_t* __restrict__ cost,
+    uint8_t* __restrict__ keep, int32_t* __restrict__ kept) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_prefix;
+  __shared__ int s_krem;
+  __shared__ int scan_scratch[33];
+  __shared__ double dred[32];
+  __shared__ int ired[32];
+  __shared__ int s_policy;
+
+  const int g = blockIdx.x;
+  const float* c = colsum + (size_t)g * n;
+  const float* bc = bandcol + (size_t)g * n;
+  const uint8_t* cl = cls + (size_t)(g / HL) * n;
+  uint8_t* kp = keep + (size_t)g * n;
+  const bool partial = k > 0 && k < n;
+
+  // --- 1. radix select of the k-th largest colsum ---------------------------
+  unsigned prefix = 0, mask = 0;
+  int krem = k;
+  if (partial) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
+      __syncthreads();
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const unsigned u = __float_as_uint(c[j]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int acc = 0, bin = 255;
+        for (; bin > 0; --bin) {
+          if (acc + (int)hist[bin] >= krem) break;
+          acc += hist[bin];
+        }
+        s_krem = krem - acc;
+        s_prefix = prefix | ((unsigned)bin << shift);
+      }
+      __syncthreads();
+      krem = s_krem;
+      prefix = s_prefix;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+  }
+  // Selected: value above the threshold, or equal to it and among the first
+  // `krem` equal values in index order.
+  const unsigned thr = prefix;
+
+  // --- 2. masses and costs --------------------------------------------------
+  double a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+  int eq_seen = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    const bool valid = j < n;
+    const float cj = valid ? c[j] : 0.f;
+    const unsigned u = __float_as_uint(cj);
+    const int is_eq = (valid && partial && u == thr) ? 1 : 0;
+    int eq_total;
+    const int eq_rank = eq_seen + block_exclusive_scan(is_eq, scan_scratch, &eq_total);
+    eq_seen += eq_total;
+    if (!valid) continue;
+    bool in_f;
+    if (k >= n) in_f = true;
+    else if (k == 0) in_f = false;
+    else in_f = (u > thr) || (is_eq && eq_rank < krem);
+    const uint8_t t = cl[j];
+    const bool s0 = t & 1, s1 = t != 0, s2 = s1 || in_f, win = j >= n - w;
+    const float bj = bc[j];
+    if (s0) { a0 += cj; ++c0; }
+    if (s1) { a1 += cj; ++c1; }
+    if (s2) { a2 += cj; a3 += (double)cj - (double)bj; ++c2; }
+    a3 += bj;
+    if (s2 || win) ++c3;
+    kp[j] = (uint8_t)((s0 ? 1 : 0) | (s1 ? 2 : 0) | (s2 ? 4 : 0) | (win ? 8 : 0));
+  }
+  a0 = block_sum(a0, dred); a1 = block_sum(a1, dred);
+  a2 = block_sum(a2, dred); a3 = block_sum(a3, dred);
+  c0 = block_sum(c0, ired); c1 = block_sum(c1, ired);
+  c2 = block_sum(c2, ired); c3 = block_sum(c3, ired);
+  if (threadIdx.x == 0) {
+    const double inv = 1.0 / (double)n;
+    const double m[5] = {a0 * inv, a1 * inv, a2 * inv, a3 * inv, 1.0};
+    const int cs[5] = {c0, c1, c2, c3, n};
+    int p = 4;
+    for (int q = 0; q < 4; ++q)
+      if (m[q] >= (double)T) { p = q; break; }
+    for (int q = 0; q < 5; ++q) {
+      mass[(size_t)g * 5 + q] = (float)m[q];
+      cost[(size_t)g * 5 + q] = cs[q];
+    }
+    policy[g] = (int8_t)p;
+    kept[g] = cs[p];
+    s_policy = p;
+  }
+  __syncthreads();
+
+  // --- 3. keep codes of the chosen policy ----------------------------------
+  const int p = s_policy;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const uint8_t bits = kp[j];
+    uint8_t code;
+    switch (p) {
+      case FG_POLICY_S: code = (bits & 1) ? FG_KEEP_STATIC : FG_KEEP_DROP; break;
+      case FG_POLICY_SP: code = (bits & 2) ? FG_KEEP_STATIC : FG_KEEP_DROP; break;
+      case FG_POLICY_SPF: code = (bits & 4) ? FG_KEEP_STATIC : FG_KEEP_DROP; break;
+      case FG_POLICY_SPFL:
+        code = (bits & 4) ? FG_KEEP_STATIC : ((bits & 8) ? FG_KEEP_WINDOW : FG_KEEP_DROP);
+        break;
+      default: code = FG_KEEP_STATIC;
+    }
+    kp[j] = code;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
+                               const int32_t* punct, int np, uint8_t* cls, cudaStream_t s) {
+  token_class_kernel<<<cdiv(count, 256), 256, 0, s>>>(ids, count, special, ns, punct, np, cls);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,
+                          const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
+                          uint8_t* keep, int32_t* kept, cudaStream_t s) {
+  select_kernel<<<pd.G, kSelThreads, 0, s>>>(colsum, bandcol, cls, pd.n, pd.HL, pd.k, pd.w, pd.T,
+                                             policy, mass, cost, keep, kept);
+  return cudaGetLastError();
+}
+
+}  // namespace fg

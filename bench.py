@@ -1,0 +1,434 @@
+"""Benchmark of the FastGen hot path on the Llama-1-7B attention shape.
+
+One step = profile every head of the prompt, plan + compact the per-head
+caches, then `steps` generation steps over those caches, all on one GPU with
+the inputs resident in HBM (Q/K/V and the caches are each larger than L2, so
+no flush is needed between steps).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama7b]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Under torchrun each rank runs its own replica (seed = rank): the heads are
+independent, so there is no data-path collective; timings are reduced with
+a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "profile+compact prompt tok/s; compressed-cache decode tok/s and HBM GB/s"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return dict(hbm=pk["hbm_gbs"], bf16=pk["bf16_tflops"],
+                    bf16_sus=pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cache_rows_per_step(cfg, policy, keep, ids, special, punct):
+    """Rows each generation step attends over, summed over heads (bookkeeping
+    for the roofline's algorithmic bytes; follows the documented placement
+    rule from the profile's outputs)."""
+    n, steps, G, HL = cfg.n, cfg.steps, cfg.G, cfg.L * cfg.H
+    w = int(np.ceil(float(np.float32(cfg.r_l)) * n))
+    b_of = np.arange(G) // HL
+    dec = ids[:, n:n + steps]
+    is_s = np.isin(dec, special)
+    is_p = np.isin(dec, punct)
+    pol = policy.astype(np.int64)[:, None]
+    st = np.where(pol == 4, True, np.where(pol == 0, is_s[b_of], (is_s | is_p)[b_of]))
+    n_static0 = (keep == 1).sum(axis=1)
+    static_t = n_static0[:, None] + np.cumsum(st, axis=1)  # [G, steps]
+    ring_ind = np.zeros((G, n + steps), dtype=np.int64)
+    ring_ind[:, :n] = keep == 2
+    ring_ind[:, n:] = (pol == 3) & ~st & (w > 0)
+    csum = np.concatenate([np.zeros((G, 1), np.int64), np.cumsum(ring_ind, axis=1)], axis=1)
+    t = np.arange(n, n + steps)
+    lo = np.maximum(t - w + 1, 0)
+    ring_t = csum[:, t + 1] - csum[:, lo]
+    ring_t = np.where(pol == 3, ring_t, 0)
+    return static_t.sum(axis=0) + ring_t.sum(axis=0), ring_t.sum(axis=0)
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from adaptive_head_kv_gb300 import fastgen as fg
+    from adaptive_head_kv_gb300.session import FastGenSession, make_params
+    from synth import CONFIGS, make_workload, punct_ids, special_ids
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda")
+    cfg = CONFIGS[args.config]
+    n, steps, G, d = cfg.n, cfg.steps, cfg.G, cfg.d
+    fg.lib()
+    w = make_workload(cfg, seed=rank)
+    pin = lambda t: t.pin_memory()
+    hQ = pin(w["Q"][:, :n].contiguous())
+    hK = pin(w["K"][:, :n].contiguous())
+    hV = pin(w["V"][:, :n].contiguous())
+    hq = pin(w["Q"][:, n:].transpose(0, 1).contiguous())
+    hk = pin(w["K"][:, n:].transpose(0, 1).contiguous())
+    hv = pin(w["V"][:, n:].transpose(0, 1).contiguous())
+    ids_np = w["ids"]
+    hids = pin(torch.from_numpy(ids_np[:, :n].copy()))
+    hdec_ids = pin(torch.from_numpy(np.ascontiguousarray(ids_np[:, n:].T)))
+    del w
+    Q, K, V = hQ.to(dev), hK.to(dev), hV.to(dev)
+    q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
+    ids, dec_ids = hids.to(dev), hdec_ids.to(dev)
+    p = make_params(cfg.B, cfg.L, cfg.H, n, d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    s = FastGenSession(p, special_ids(rank), punct_ids(rank), steps, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step(record):
+        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)] if record else None
+        e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0.record(stream)
+        s.profile(Q, K, ids)
+        e1.record(stream)
+        s.compact(K, V)
+        e2.record(stream)
+        for st in range(steps):
+            if record:
+                dec_ev[st][0].record(stream)
+            s.decode(q[st], k[st], v[st], dec_ids[st], n + st)
+            if record:
+                dec_ev[st][1].record(stream)
+        e3.record(stream)
+        return e0, e1, e2, e3, dec_ev
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        one_step(False)
+    barrier()
+    per = []
+    dec_ms = np.zeros(steps)
+    with Clocks(torch.cuda.current_device()) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            per.append(one_step(True))
+        t_end.record(stream)
+        barrier()
+    for ev in per:
+        for st in range(steps):
+            dec_ms[st] += ev[4][st][0].elapsed_time(ev[4][st][1])
+    total_ms = t_start.elapsed_time(t_end)
+    prof_ms = np.mean([a.elapsed_time(b) for a, b, c, e, _ in per])
+    comp_ms = np.mean([b.elapsed_time(c) for a, b, c, e, _ in per])
+    decode_ms = np.mean([c.elapsed_time(e) for a, b, c, e, _ in per])
+    step_ms = np.mean([a.elapsed_time(e) for a, b, c, e, _ in per])
+    dec_ms /= args.steps
+    assert fg.fastgen_read_error(s.dev_err) == fg.FG_OK
+
+    # algorithmic work
+    policy = s.policy.cpu().numpy()
+    keep = s.keep.cpu().numpy()
+    rows_t, ring_t = cache_rows_per_step(cfg, policy, keep, ids_np, special_ids(rank),
+                                         punct_ids(rank))
+    eb = 2 if cfg.dtype == "bf16" else 4
+    dec_bytes_t = rows_t * d * 2 * eb + G * d * eb * 4 + ring_t * 4 + G * 40
+    dec_gbs = dec_bytes_t.sum() / (dec_ms.sum() * 1e-3) / 1e9
+    prof_flops = 2.0 * n * (n + 1) * d * G
+    kept_rows = int((keep != 0).sum())
+    comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + G * 40
+    return dict(cfg=cfg, prof_ms=prof_ms, comp_ms=comp_ms, decode_ms=decode_ms, step_ms=step_ms,
+                total_ms=total_ms, dec_ms=dec_ms, dec_bytes=float(dec_bytes_t.mean()),
+                dec_gbs=dec_gbs, prof_flops=prof_flops, comp_bytes=comp_bytes,
+                kept_frac=kept_rows / (G * n), clocks=clk.summary(),
+                e2e=run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream))
+
+
+def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
+    """Same metric through the public calls with host buffers: every step
+    copies its inputs from pinned host memory and reads its results back."""
+    import torch
+
+    dev = torch.device("cuda")
+    n, steps = cfg.n, cfg.steps
+    hpol = torch.empty(s.G, dtype=torch.int8).pin_memory()
+    hout = torch.empty(steps, s.G, cfg.d, dtype=s.tdtype).pin_memory()
+    Q, K, V = (torch.empty_like(x, device=dev) for x in (hQ, hK, hV))
+    ids = torch.empty_like(hids, device=dev)
+    qs, ks, vs = (torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev) for _ in range(3))
+    did = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+
+    def step():
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        Q.copy_(hQ, non_blocking=True)
+        K.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        ids.copy_(hids, non_blocking=True)
+        s.prefill(Q, K, V, ids)
+        hpol.copy_(s.policy, non_blocking=True)
+        b.record(stream)
+        for st in range(steps):
+            qs.copy_(hq[st], non_blocking=True)
+            ks.copy_(hk[st], non_blocking=True)
+            vs.copy_(hv[st], non_blocking=True)
+            did.copy_(hdec_ids[st], non_blocking=True)
+            s.decode(qs, ks, vs, did, n + st)
+            hout[st].copy_(s.out, non_blocking=True)
+        c.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), b.elapsed_time(c)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    pre, dec = zip(*[step() for _ in range(max(1, min(args.steps, 3)))])
+    eb = hQ.element_size()
+    return dict(prefill_ms=float(np.mean(pre)), decode_ms=float(np.mean(dec)),
+                h2d=3 * hQ.numel() * eb + hids.numel() * 4,
+                d2h=s.G,
+                dec_h2d=steps * (3 * s.G * cfg.d * eb + cfg.B * 4),
+                dec_d2h=steps * s.G * cfg.d * eb)
+
+
+def oracle_sample(cfg, heads, seed=0):
+    """Times the oracle (as it stands) on `heads` of the workload: profile,
+    compaction and all decode steps per head.  Returns (profile+compact s,
+    decode s) summed over the sampled heads."""
+    from oracle import fastgen_oracle as O
+    from synth import make_workload, punct_ids, special_ids
+
+    w = make_workload(cfg, seed, heads=heads, threads=4)
+    n, steps = cfg.n, cfg.steps
+    T = float(np.float32(cfg.T))
+    t_pc = t_dec = 0.0
+    for i, g in enumerate(heads):
+        b = int(g) // (cfg.L * cfg.H)
+        Qa, Ka, Va = (w[x][i].double().numpy() for x in "QKV")
+        ids = w["ids"][b]
+        t0 = time.perf_counter()
+        r = O.profile_head(Qa[:n], Ka[:n], ids, special_ids(seed), punct_ids(seed), T,
+                           cfg.r_l, cfg.r_f)
+        O.compact_head(Ka[:n], Va[:n], r["keep"])
+        t1 = time.perf_counter()
+        O.decode_head(r["policy"], r["keep"], n, r["w"], ids, Qa, Ka, Va, special_ids(seed),
+                      punct_ids(seed), steps)
+        t2 = time.perf_counter()
+        t_pc += t1 - t0
+        t_dec += t2 - t1
+    return t_pc, t_dec
+
+
+def host_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, n_heads=8):
+    rng = np.random.default_rng(123)
+    heads = sorted(rng.choice(cfg.G, size=min(n_heads, cfg.G), replace=False).tolist())
+    t_pc, t_dec = oracle_sample(cfg, heads)
+    scale = cfg.G / len(heads)
+    return {"value": cfg.B * cfg.n / (t_pc * scale), "unit": "tok/s", "cores": host_threads(),
+            "kind": "oracle",
+            "decode_tok_s": cfg.B * cfg.steps / (t_dec * scale),
+            "sample": f"{len(heads)} of {cfg.G} heads of {cfg.name} (profile+compact+{cfg.steps} "
+                      f"decode steps each, {t_pc + t_dec:.1f} s), extrapolated linearly in heads"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="llama7b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    from synth import CONFIGS
+
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, cfg, world)
+        return
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    r = run_ours(args, rank, world)
+    mine = torch.tensor([r["step_ms"], r["prof_ms"] + r["comp_ms"], r["decode_ms"],
+                         r["dec_ms"].mean()], dtype=torch.float64, device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(mine, op=torch.distributed.ReduceOp.MAX)
+    step_ms, prompt_ms, decode_ms, dec_launch_ms = mine.tolist()
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    pk = load_peaks()
+    prompt_tok_s = world * cfg.B * cfg.n / (prompt_ms * 1e-3)
+    decode_tok_s = world * cfg.B * cfg.steps / (decode_ms * 1e-3)
+    dec_ach = r["dec_bytes"] / (dec_launch_ms * 1e-3) / 1e9
+    prof_ach = r["prof_flops"] / (r["prof_ms"] * 1e-3) / 1e12
+    dec_roof = {"kernel": "fastgen_decode_attn (split + combine)", "bound": "hbm",
+                "achieved": dec_ach, "peak": pk["hbm"], "unit": "GB/s", "frac": dec_ach / pk["hbm"],
+                "traffic": None, "peak_source": pk["src"],
+                "algorithmic_bytes_per_launch": r["dec_bytes"]}
+    prof_roof = {"kernel": "fastgen_profile (both passes + select)", "bound": "tensor",
+                 "achieved": prof_ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                 "frac": prof_ach / pk["bf16"], "traffic": None, "peak_source": pk["src"],
+                 "algorithmic_flops_per_launch": r["prof_flops"]}
+    dec_total = r["decode_ms"]
+    dominant, other = (dec_roof, prof_roof) if dec_total >= r["prof_ms"] else (prof_roof, dec_roof)
+    e = r["e2e"]
+    out = {
+        "metric": METRIC, "value": prompt_tok_s, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded generator, planted head types; no weights or datasets)",
+        "config": {"workload": f"{cfg.name}: B={cfg.B} L={cfg.L} H={cfg.H} d={cfg.d} n={cfg.n} "
+                               f"decode_steps={cfg.steps} T={cfg.T} r_l={cfg.r_l} r_f={cfg.r_f}",
+                   "G": cfg.G, "parallelism": f"replicas x{world}",
+                   "l2": "inputs and caches larger than L2 (no flush)",
+                   "step": "profile + plan + compact + all decode steps"},
+        "decode_tok_s": decode_tok_s, "decode_hbm_gbs": r["dec_gbs"],
+        "phases_ms": {"profile": r["prof_ms"], "compact_plan": r["comp_ms"],
+                      "decode_all_steps": r["decode_ms"], "decode_per_step": dec_launch_ms},
+        "kept_fraction": r["kept_frac"],
+        "roofline": dominant, "roofline_other": other,
+        "clocks": r["clocks"],
+        "e2e": {"value": world * cfg.B * cfg.n / (e["prefill_ms"] * 1e-3), "unit": "tok/s",
+                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                "decode_tok_s": world * cfg.B * cfg.steps / (e["decode_ms"] * 1e-3),
+                "decode_h2d_bytes_per_step": e["dec_h2d"],
+                "decode_d2h_bytes_per_step": e["dec_d2h"]},
+        "gpu_launches": args.steps * (fg_launches("profile") + fg_launches("plan")
+                                      + fg_launches("compact") + cfg.steps * fg_launches("decode")),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def fg_launches(call):
+    from adaptive_head_kv_gb300.fastgen import LAUNCHES
+
+    return LAUNCHES[call]
+
+
+def run_reference(args, cfg, world):
+    """The oracle timed as it stands on the host cores, on bounded samples of
+    the same workload, reported in the same metric."""
+    heads_per_step = 2
+    rng = np.random.default_rng(7)
+    for _ in range(args.warmup):
+        pass  # the oracle has nothing to warm up; warm-up steps are not timed
+    t_pc = t_dec = 0.0
+    sampled = 0
+    for _ in range(args.steps):
+        heads = sorted(rng.choice(cfg.G, size=heads_per_step, replace=False).tolist())
+        a, b = oracle_sample(cfg, heads)
+        t_pc += a
+        t_dec += b
+        sampled += heads_per_step
+    scale = cfg.G / sampled
+    value = cfg.B * cfg.n / (t_pc * scale) * 1.0
+    step_ms = (t_pc + t_dec) * scale / args.steps * 1e3
+    cores = host_threads()
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded generator)",
+           "config": {"workload": f"{cfg.name}", "G": cfg.G,
+                      "step": f"{heads_per_step} sampled heads, extrapolated to all {cfg.G}"},
+           "decode_tok_s": cfg.B * cfg.steps / (t_dec * scale),
+           "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{heads_per_step} heads per step x {args.steps} steps of "
+                                      f"{cfg.name}, extrapolated linearly in heads"},
+           "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

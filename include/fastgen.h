@@ -1,0 +1,215 @@
+/*
+ * fastgen.h -- C ABI of the GB300 (sm_103a) FastGen hot path.
+ *
+ * FastGen ("Model Tells You What to Discard: Adaptive KV Cache Compression
+ * for LLMs", ICLR 2024; hyper.ai paper summaries in Chinese and Korean/English,
+ * section Method) compresses the KV cache per attention head in two phases:
+ *   1. prompt encoding: profile every head on A = softmax(Q K^T) and pick the
+ *      cheapest hybrid policy of the shortlist {special, special+punct,
+ *      special+punct+frequent, special+punct+frequent+local, full} whose kept
+ *      attention is within the recover ratio T (eq. (C*));
+ *   2. generation: keep a head-specific cache K_C, V_C = f(K, V, C), append
+ *      new keys/values to it by the same policy, and attend over it.
+ *
+ * The library covers three calls of that path: fastgen_profile (phase 1),
+ * fastgen_compact_plan + fastgen_compact (building K_C, V_C) and
+ * fastgen_decode_attn (one generation step for every head).
+ *
+ * Conventions shared by every entry point
+ *   - Heads are a flat index g = (b*L + l)*H + h over G = B*L*H instances.
+ *   - All array arguments are DEVICE pointers owned by the caller unless
+ *     marked HOST; the library never allocates, frees or keeps memory
+ *     between calls, and has no global state.  Scratch memory is passed in
+ *     as `workspace`.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on it unless stated otherwise.
+ *   - Argument errors are detected on the host before any launch and
+ *     returned as a negative fg_status; nothing is launched then.  Launch
+ *     failures return FG_ECUDA.  No call traps, asserts or aborts on device.
+ *   - Element types: Q/K/V/q/out and the K/V pools are bf16 (FG_BF16) or
+ *     fp32 (FG_FP32) per fg_params.dtype; head dim d is 64 or 128; every
+ *     K/V/Q row is contiguous (row-major [.., d]) and 16-byte aligned.
+ */
+#ifndef FASTGEN_H
+#define FASTGEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FG_OK = 0,
+  FG_EINVAL = -1,      /* bad size, ratio, threshold, null or misaligned pointer */
+  FG_EDTYPE = -2,      /* dtype or head dim not supported */
+  FG_EWORKSPACE = -3,  /* workspace / plan / pool buffer too small */
+  FG_ECAPACITY = -4,   /* a head ran out of reserved cache rows while appending */
+  FG_ECUDA = -5        /* a CUDA runtime call or launch failed */
+} fg_status;
+
+typedef enum { FG_BF16 = 0, FG_FP32 = 1 } fg_dtype;
+
+/* Policy ids, in the shortlist order of eq. (C*). */
+enum {
+  FG_POLICY_S = 0,    /* special */
+  FG_POLICY_SP = 1,   /* special + punct */
+  FG_POLICY_SPF = 2,  /* special + punct + frequent */
+  FG_POLICY_SPFL = 3, /* special + punct + frequent + local */
+  FG_POLICY_FULL = 4  /* full cache */
+};
+
+/* Keep-mask codes written by fastgen_profile. */
+enum {
+  FG_KEEP_DROP = 0,   /* position not in the compressed cache */
+  FG_KEEP_STATIC = 1, /* kept for the whole generation (special/punct/frequent, or full) */
+  FG_KEEP_WINDOW = 2  /* kept only while inside the local window (SPFL heads) */
+};
+
+typedef struct {
+  int32_t B, L, H; /* batch, layers, heads per layer: G = B*L*H */
+  int32_t n;       /* prompt length, >= 1 */
+  int32_t d;       /* head dim: 64 or 128 */
+  int32_t dtype;   /* fg_dtype */
+  float T;         /* recover ratio, 0 < T <= 1 (eq. (C*)) */
+  float r_l;       /* local ratio in [0, 1]: window w = ceil(r_l * n) */
+  float r_f;       /* frequent ratio in [0, 1]: k = ceil(r_f * n) keys */
+  float scale;     /* score scale s in softmax(s Q K^T); 0 selects 1/sqrt(d) */
+} fg_params;
+
+/* One head's compressed cache inside the pooled K/V buffers. */
+typedef struct {
+  int64_t off;        /* first pool row of the never-evicted segment */
+  int32_t n_static;   /* rows currently used in that segment */
+  int32_t static_cap; /* rows reserved for it */
+  int64_t win_off;    /* first pool row of the window ring */
+  int32_t w;          /* ring rows (window size; 0 unless policy is SPFL) */
+  int32_t policy;     /* FG_POLICY_* */
+  int32_t work_off;   /* first decode work item of this head */
+  int32_t n_work;     /* decode work items of this head */
+} fg_head_desc;
+
+typedef struct {
+  int64_t pool_rows;     /* rows the K, V and position pools must hold */
+  int32_t n_work;        /* decode work items of the plan */
+  int32_t rows_per_work; /* cache rows covered by one decode work item */
+} fg_plan_info;
+
+/* Human-readable text of a status code (static storage). */
+const char* fastgen_status_string(fg_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t fastgen_version(void);
+
+/* ------------------------------------------------------------------------
+ * Phase 1: prompt profiling (Method: A = softmax(QK^T), base policies,
+ * shortlist, eq. (C*)).
+ *
+ * For every head g, with s the scale and the causal mask (row i sees j <= i):
+ *   A_ij      = softmax_j(s q_i . k_j)
+ *   colsum_j  = sum_i A_ij                       (cumulative attention score)
+ *   Spec/Punc = prompt positions whose token id is in special_ids / punct_ids
+ *   Freq      = top-k keys by colsum, k = ceil(r_f n), ties to the lower index
+ *   Local_i   = {j : i - w < j <= i}, w = ceil(r_l n)
+ *   mass[g,p] = (1/n) sum_i sum_{j in K_i^p} A_ij for the nested per-row sets
+ *               K^0 = Spec, K^1 = K^0 u Punc, K^2 = K^1 u Freq,
+ *               K_i^3 = K^2 u Local_i; mass[g,4] = 1.  1 - mass is the mean
+ *               half-L1 distance of eq. (C*).
+ *   cost[g,p] = cache rows kept at the end of the prompt: |K^p| for p <= 2,
+ *               |K^2 u {n-w .. n-1}| for p = 3, n for p = 4.
+ *   policy[g] = the first p (= cheapest) with mass[g,p] >= T.
+ *   keep[g,j] = FG_KEEP_* code of position j in the chosen policy's cache.
+ *   kept[g]   = cost[g, policy[g]].
+ * Ratios are evaluated as ceil(r * n) exactly on the float value of r.
+ *
+ * Arguments:
+ *   Q, K        [G, n, d] dtype, row-major, 16-byte aligned.
+ *   token_ids   [B, n] int32 prompt token ids.
+ *   special_ids [n_special] int32, punct_ids [n_punct] int32 (0 <= counts <= 4096;
+ *               a count of 0 allows a NULL pointer).
+ *   policy [G] int8, mass [G,5] float, cost [G,5] int32, colsum [G,n] float,
+ *   keep [G,n] uint8, kept [G] int32: outputs.
+ *   workspace: >= fastgen_profile_workspace_bytes(p) bytes, 256-byte aligned.
+ * Errors: FG_EINVAL for G, n < 1, T outside (0,1], ratios outside [0,1],
+ * null/misaligned pointers; FG_EDTYPE for other d or dtype; FG_EWORKSPACE.
+ * ------------------------------------------------------------------------ */
+size_t fastgen_profile_workspace_bytes(const fg_params* p);
+
+fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
+                          const int32_t* token_ids, const int32_t* special_ids,
+                          int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                          int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                          uint8_t* keep, int32_t* kept, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Compaction, step 1: the pool layout (Method: K_C, V_C = f(K, V, C)).
+ *
+ * From policy [G] and cost [G,5] (outputs of fastgen_profile) it writes, into
+ * the device buffer `plan` (>= fastgen_plan_bytes bytes, 256-byte aligned):
+ * G fg_head_desc records followed by the decode work list.  Each head gets a
+ * never-evicted segment of (kept static rows + max_new_tokens) rows and, for
+ * SPFL heads, a ring of w rows for the sliding window.  The totals are
+ * written to *info (HOST pointer).  This call is SYNCHRONOUS: it waits on
+ * `stream` to return the totals.
+ * ------------------------------------------------------------------------ */
+size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens);
+
+fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const int32_t* cost,
+                               int32_t max_new_tokens, void* plan, size_t plan_bytes,
+                               fg_plan_info* info, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Compaction, step 2: gather the kept prompt rows into the pools.
+ *
+ * K, V [G, n, d] dtype; keep [G, n] from fastgen_profile; plan and *info
+ * (HOST pointer) from fastgen_compact_plan.  Writes K_pool, V_pool
+ * [pool_rows, d] dtype and pos_pool [pool_rows] int32 (absolute position of
+ * each row, -1 = empty).  Never-evicted rows are stored in position order;
+ * window rows sit at ring slot (position mod w).
+ * Errors: FG_EWORKSPACE if pool_rows < info->pool_rows.
+ * ------------------------------------------------------------------------ */
+fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, const uint8_t* keep,
+                          const void* plan, const fg_plan_info* info, void* K_pool,
+                          void* V_pool, int32_t* pos_pool, int64_t pool_rows, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Generation step for every head (Method: head-specific caches, appends,
+ * policy reused from the prompt).
+ *
+ * The new token at absolute position pos (>= n) with id new_ids[b] is placed
+ * by its head's policy: full -> appended; special/punct-containing policies
+ * append it to the never-evicted segment when its id is special (or, except
+ * for the special-only policy, punctuation); SPFL heads otherwise put it in
+ * the window ring at slot pos mod w, evicting the row that left the window.
+ * The frequent set stays as profiled.  Then
+ *   out[g] = sum_{j in cache_g} softmax_j(s q_g . k_j) v_j   (zeros if empty)
+ * over the cache after placement.
+ *
+ * Arguments: plan and *info (HOST pointer) from fastgen_compact_plan; pools
+ * from fastgen_compact (updated in place); q, k_new, v_new [G, d] dtype;
+ * new_ids [B] int32; id sets as in fastgen_profile; out [G, d] dtype;
+ * workspace >= fastgen_decode_workspace_bytes(p, info).  dev_err: device
+ * int32 that the call ORs with 1 when a head had no free reserved row (that
+ * token is then not stored); read it with fastgen_read_error.
+ * ------------------------------------------------------------------------ */
+size_t fastgen_decode_workspace_bytes(const fg_params* p, const fg_plan_info* info);
+
+fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info* info,
+                              void* K_pool, void* V_pool, int32_t* pos_pool, const void* q,
+                              const void* k_new, const void* v_new, const int32_t* new_ids,
+                              const int32_t* special_ids, int32_t n_special,
+                              const int32_t* punct_ids, int32_t n_punct, int32_t pos,
+                              void* out, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, void* stream);
+
+/* Synchronously reads the device flag written by fastgen_decode_attn and
+ * maps it to a status (FG_OK or FG_ECAPACITY).  Waits on `stream`. */
+fg_status fastgen_read_error(const int32_t* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FASTGEN_H */

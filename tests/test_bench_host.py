@@ -1,0 +1,31 @@
+"""Host-side bookkeeping of bench.py: the per-step cache sizes used for the
+decode roofline equal the oracle's cache sets."""
+import numpy as np
+
+import bench
+from oracle import fastgen_oracle as O
+from synth import CONFIGS, make_workload, punct_ids, special_ids
+
+
+def test_cache_rows_match_oracle():
+    cfg = CONFIGS["tiny"].with_(L=2, H=4, n=100, steps=30, r_l=0.2)
+    w = make_workload(cfg, threads=1)
+    T = float(np.float32(cfg.T))
+    policy, keep, sizes = [], [], np.zeros(cfg.steps, dtype=np.int64)
+    for g in range(cfg.G):
+        Qa, Ka, Va = (w[x][g].double().numpy() for x in "QKV")
+        r = O.profile_head(Qa[:cfg.n], Ka[:cfg.n], w["ids"][0], special_ids(), punct_ids(), T,
+                           cfg.r_l, cfg.r_f)
+        policy.append(r["policy"])
+        keep.append(r["keep"])
+        static = [int(j) for j in np.nonzero(r["keep"] == O.KEEP_STATIC)[0]]
+        for st in range(cfg.steps):
+            t = cfg.n + st
+            tau = int(w["ids"][0][t])
+            if O.stores_static(r["policy"], tau in special_ids(), tau in punct_ids()):
+                static.append(t)
+            sizes[st] += len(O.decode_positions(r["policy"], static, r["w"], t))
+    rows, ring = bench.cache_rows_per_step(cfg, np.array(policy), np.array(keep), w["ids"],
+                                           special_ids(), punct_ids())
+    assert np.array_equal(rows, sizes)
+    assert (ring >= 0).all()

@@ -1,0 +1,104 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle on the same
+seeded workloads (tolerances in parity_util)."""
+import numpy as np
+import pytest
+import torch
+
+from synth import CONFIGS, head_types
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from parity_util import compare, run_gpu, sample_heads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    fg.lib()  # raises if the CUDA library is missing
+
+
+def check_all(cfg, T=None, max_new=None):
+    gpu = run_gpu(cfg, T=T, max_new=max_new)
+    rep = compare(cfg, gpu, list(range(cfg.G)), T=T)
+    assert gpu["dev_err"] == 0
+    assert rep["decode_checked"] >= max(1, rep["checked"] // 2), rep
+    return gpu, rep
+
+
+def test_tiny_fp32_all_heads():
+    cfg = CONFIGS["tiny"]
+    gpu, rep = check_all(cfg)
+    assert list(gpu["policy"]) [0] == 0 and gpu["policy"][2] == 3
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("bf16_d128_ragged", dict(dtype="bf16", d=128, L=2, H=6, n=300, steps=40, one_of_each=False)),
+    ("bf16_d64", dict(dtype="bf16", d=64, L=2, H=4, n=257, steps=30)),
+    ("fp32_d128", dict(dtype="fp32", d=128, L=1, H=8, n=200, steps=20, one_of_each=False)),
+    ("bf16_two_seqs", dict(dtype="bf16", d=128, B=2, L=1, H=4, n=190, steps=25)),
+])
+def test_small_shapes(name, kw):
+    check_all(CONFIGS["tiny"].with_(**kw))
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("n1", dict(n=1, steps=5)),
+    ("n2", dict(n=2, steps=5)),
+    ("no_window", dict(r_l=0.0)),
+    ("no_frequent", dict(r_f=0.0)),
+    ("everything", dict(r_l=1.0, r_f=1.0)),
+    ("T_one", dict(T=1.0)),
+    ("T_small", dict(T=1e-6)),
+    ("window_tiny", dict(r_l=0.01, n=150, steps=40)),
+])
+def test_edge_cases(name, kw):
+    base = CONFIGS["tiny"].with_(dtype="bf16", d=128, n=129, steps=12)
+    check_all(base.with_(**kw))
+
+
+def test_capacity_overflow_sets_flag():
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, n=64, steps=3)
+    gpu = run_gpu(cfg, max_new=0)
+    assert gpu["dev_err"] == 1  # the full-cache head had no reserved row
+    assert fg.fastgen_read_error(gpu["session"].dev_err) == fg.FG_ECAPACITY
+    # heads that stored nothing new are unaffected
+    d = gpu["desc1"]
+    for g in range(cfg.G):
+        assert d[g].n_static == gpu["desc0"][g].n_static
+
+
+@pytest.mark.parametrize("name,kw,T", [
+    ("llama13b_shape", dict(B=1, L=2, H=6, steps=48), None),
+    ("llama65b_shape_T090", dict(B=2, L=2, H=3, steps=40), 0.90),
+    ("llama65b_shape_T098", dict(B=2, L=2, H=3, steps=40), 0.98),
+    ("long8k_shape", dict(B=1, L=1, H=6, steps=24), None),
+])
+def test_config_shapes_reduced_heads(name, kw, T):
+    base = {"llama13b_shape": "llama13b", "llama65b_shape_T090": "llama65b",
+            "llama65b_shape_T098": "llama65b", "long8k_shape": "long8k"}[name]
+    cfg = CONFIGS[base].with_(**kw)
+    check_all(cfg, T=T)
+
+
+def test_llama7b_full_size_sampled():
+    """The bench workload at full size: every head's invariants, sampled
+    heads against the oracle (all decode steps)."""
+    cfg = CONFIGS["llama7b"]
+    gpu = run_gpu(cfg, check_pools=True)
+    heads = sample_heads(cfg, head_types(cfg), 24)
+    rep = compare(cfg, gpu, heads)
+    assert gpu["dev_err"] == 0
+    assert rep["decode_checked"] >= 16, rep
+    kept_frac = gpu["kept"].sum() / (cfg.G * cfg.n)
+    assert 0.3 < kept_frac < 0.8, kept_frac
+
+
+def test_deterministic_rerun():
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=4, n=300, steps=8)
+    a, b = run_gpu(cfg), run_gpu(cfg)
+    for key in ("policy", "mass", "colsum", "keep", "out"):
+        assert np.array_equal(a[key], b[key]), key
