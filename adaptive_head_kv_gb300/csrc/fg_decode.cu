@@ -91,10 +91,16 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, gl = lane % LPR;
+  // fp32 inputs: the dot is accumulated in fp64 and scaled once, so that
+  // rounding does not perturb the scores key by key (the fp32 path is held
+  // to 1e-5 on the outputs); bf16 inputs use an fp32 dot on a pre-scaled q.
+  constexpr bool kWide = sizeof(T) == 4;
   float qf[E];
   load16((const T*)a.q + (size_t)g * D + gl * E, qf);
+  if (!kWide) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) qf[e] *= sl2;
+    for (int e = 0; e < E; ++e) qf[e] *= sl2;
+  }
   float m = FG_NEG_INF, l = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
@@ -124,11 +130,21 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
     for (int u = 0; u < kUnroll; ++u) {
       float f[E];
       unpack16(kv[u], f, (const T*)nullptr);
-      float dot = 0.f;
+      float dot;
+      if (kWide) {
+        double dd = 0.0;
 #pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(qf[e], f[e], dot);
+        for (int e = 0; e < E; ++e) dd = fma((double)qf[e], (double)f[e], dd);
 #pragma unroll
-      for (int o = LPR / 2; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        for (int o = LPR / 2; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+        dot = (float)(dd * (double)sl2);
+      } else {
+        dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qf[e], f[e], dot);
+#pragma unroll
+        for (int o = LPR / 2; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      }
       s[u] = ok[u] ? dot : FG_NEG_INF;
       mloc = fmaxf(mloc, s[u]);
     }

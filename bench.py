@@ -298,7 +298,7 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, n_heads=8):
+def cpu_baseline(cfg, n_heads=48):
     rng = np.random.default_rng(123)
     heads = sorted(rng.choice(cfg.G, size=min(n_heads, cfg.G), replace=False).tolist())
     t_pc, t_dec = oracle_sample(cfg, heads)
