@@ -26,7 +26,11 @@ EXPORTS = (
     "fastgen_status_string", "fastgen_version", "fastgen_profile_workspace_bytes",
     "fastgen_profile", "fastgen_plan_bytes", "fastgen_compact_plan", "fastgen_compact",
     "fastgen_decode_workspace_bytes", "fastgen_decode_attn", "fastgen_read_error",
+    "fastgen_decode_attn_noalloc",
 )
+
+# size of the library-held scratch array used by fastgen_decode_attn_noalloc
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 class Params(ctypes.Structure):
@@ -73,6 +77,9 @@ _SIGS = {
                                            _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                            _P, _P, _SZ, _P, _P]),
     "fastgen_read_error": (ctypes.c_int, [_P, _P]),
+    "fastgen_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(Params), _P,
+                                                   ctypes.POINTER(PlanInfo), _P, _P, _P, _P, _P,
+                                                   _P, _P, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
 }
 
 
@@ -180,3 +187,16 @@ def fastgen_decode_attn(params, plan, info, K_pool, V_pool, pos_pool, q, k_new, 
 
 def fastgen_read_error(dev_err, stream=None) -> int:
     return lib().fastgen_read_error(_ptr(dev_err), _stream(stream))
+
+
+def fastgen_decode_attn_noalloc(params, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new,
+                                new_ids, special_ids, punct_ids, pos, out, dev_err,
+                                stream=None) -> None:
+    """fastgen_decode_attn without a workspace: for callers that cannot
+    allocate device memory while decoding (the scratch is a fixed array held
+    by the library; calls must not overlap on the GPU)."""
+    _check(lib().fastgen_decode_attn_noalloc(
+        ctypes.byref(params), _ptr(plan), ctypes.byref(info), _ptr(K_pool), _ptr(V_pool),
+        _ptr(pos_pool), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(new_ids), _ptr(special_ids),
+        _count(special_ids), _ptr(punct_ids), _count(punct_ids), int(pos), _ptr(out),
+        _ptr(dev_err), _stream(stream)), "fastgen_decode_attn_noalloc")

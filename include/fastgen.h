@@ -204,6 +204,41 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
                               void* out, void* workspace, size_t workspace_bytes,
                               int32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * fastgen_decode_attn for callers that cannot allocate device memory.
+ * (The paper has no counterpart: this is a deployment convenience.)
+ *
+ * Some callers cannot call cudaMalloc when they decode: a serving engine that
+ * gives all free device memory to its own pool at start-up (a new allocation
+ * fails or undercuts that pool), a plug-in whose host framework owns every
+ * allocation, or a latency-bound loop that cannot pay for cudaMalloc's
+ * implicit synchronisation.  This variant takes the same arguments as
+ * fastgen_decode_attn minus `workspace`/`workspace_bytes` and allocates
+ * nothing: its scratch (the split-K partial results) is a fixed array of
+ * FASTGEN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *   - The first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and produce wrong results, so issue
+ *     them in order on one stream.  Nothing in the array has to start at
+ *     zero: a call writes every entry it later reads.
+ *   - Returns FG_EWORKSPACE when the plan needs more scratch than the array
+ *     holds, i.e. fastgen_decode_workspace_bytes(p, info) >
+ *     FASTGEN_NOALLOC_SCRATCH_BYTES (about 16,000 decode work items at
+ *     d = 128); other errors as fastgen_decode_attn.
+ * ------------------------------------------------------------------------ */
+#define FASTGEN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+fg_status fastgen_decode_attn_noalloc(const fg_params* p, void* plan, const fg_plan_info* info,
+                                      void* K_pool, void* V_pool, int32_t* pos_pool,
+                                      const void* q, const void* k_new, const void* v_new,
+                                      const int32_t* new_ids, const int32_t* special_ids,
+                                      int32_t n_special, const int32_t* punct_ids,
+                                      int32_t n_punct, int32_t pos, void* out,
+                                      int32_t* dev_err, void* stream);
+
 /* Synchronously reads the device flag written by fastgen_decode_attn and
  * maps it to a status (FG_OK or FG_ECAPACITY).  Waits on `stream`. */
 fg_status fastgen_read_error(const int32_t* dev_err, void* stream);
