@@ -118,7 +118,7 @@ def cache_rows_per_step(cfg, policy, keep, ids, special, punct):
     return static_t.sum(axis=0) + ring_t.sum(axis=0), ring_t.sum(axis=0)
 
 
-def run_ours(args, rank, world):
+def run_ours(args, cfg, rank, world):
     import torch
 
     from adaptive_head_kv_gb300 import fastgen as fg
@@ -127,7 +127,6 @@ def run_ours(args, rank, world):
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     dev = torch.device("cuda")
-    cfg = CONFIGS[args.config]
     n, steps, G, d = cfg.n, cfg.steps, cfg.G, cfg.d
     fg.lib()
     w = make_workload(cfg, seed=rank)
@@ -318,12 +317,16 @@ def main():
     ap.add_argument("--config", default="llama7b")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (smaller cases for profiler captures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     from synth import CONFIGS
 
     cfg = CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.with_(L=args.layers, name=f"{cfg.name}_L{args.layers}")
     if args.impl == "reference":
         if rank != 0:
             return
@@ -334,7 +337,7 @@ def main():
 
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    r = run_ours(args, rank, world)
+    r = run_ours(args, cfg, rank, world)
     mine = torch.tensor([r["step_ms"], r["prof_ms"] + r["comp_ms"], r["decode_ms"],
                          r["dec_ms"].mean()], dtype=torch.float64, device="cuda")
     if world > 1:
