@@ -77,6 +77,7 @@ const char* fastgen_status_string(fg_status s) {
     case FG_EWORKSPACE: return "workspace, plan or pool buffer too small";
     case FG_ECAPACITY: return "a head ran out of reserved cache rows";
     case FG_ECUDA: return "CUDA error";
+    case FG_EDEVICE: return "a device-side wait timed out; results of that call are invalid";
   }
   return "unknown status";
 }
@@ -86,7 +87,8 @@ int32_t fastgen_version(void) { return 100; }
 size_t fastgen_profile_workspace_bytes(const fg_params* p) {
   if (check_params(p) != FG_OK) return 0;
   const size_t G = (size_t)p->B * p->L * p->H, n = p->n;
-  return 2 * align_up(G * n * sizeof(float)) + align_up((size_t)p->B * n);
+  return align_up(G * fg::lse_ld(p->n) * sizeof(float)) + align_up(G * n * sizeof(float)) +
+         align_up((size_t)p->B * n);
 }
 
 fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
@@ -94,28 +96,36 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
                           int8_t* policy, float* mass, int32_t* cost, float* colsum,
                           uint8_t* keep, int32_t* kept, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+                          size_t workspace_bytes, int32_t* dev_err, void* stream) {
   fg_status st = check_params(p);
   if (st != FG_OK) return st;
   if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
   if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
   if (!Q || !K || !token_ids || !policy || !mass || !cost || !colsum || !keep || !kept ||
-      !workspace)
+      !workspace || !dev_err)
     return FG_EINVAL;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(workspace, kAlign) || !aligned(mass, 4) ||
-      !aligned(cost, 4) || !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4))
+      !aligned(cost, 4) || !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4) ||
+      !aligned(dev_err, 4))
     return FG_EINVAL;
   if (workspace_bytes < fastgen_profile_workspace_bytes(p)) return FG_EWORKSPACE;
   const fg::ProfileDims pd = dims(p);
   const size_t Gn = (size_t)pd.G * pd.n;
+  const int ld = fg::lse_ld(pd.n);
   char* ws = (char*)workspace;
   float* lse2 = (float*)ws;
-  float* bandcol = (float*)(ws + align_up(Gn * sizeof(float)));
-  uint8_t* cls = (uint8_t*)(ws + 2 * align_up(Gn * sizeof(float)));
+  const size_t lse_bytes = align_up((size_t)pd.G * ld * sizeof(float));
+  float* bandcol = (float*)(ws + lse_bytes);
+  uint8_t* cls = (uint8_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
                                          punct_ids, n_punct, cls, s);
-  if (e == cudaSuccess) e = fg::launch_profile_simt(pd, Q, K, lse2, colsum, bandcol, s);
+  if (e == cudaSuccess) {
+    if (fg::profile_tc_supported(pd))
+      e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, dev_err, s);
+    else
+      e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
+  }
   if (e == cudaSuccess)
     e = fg::launch_select(pd, colsum, bandcol, cls, policy, mass, cost, keep, kept, s);
   return cuda_status(e);
@@ -234,6 +244,7 @@ fg_status fastgen_read_error(const int32_t* dev_err, void* stream) {
   if (cudaMemcpyAsync(&h, dev_err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return FG_ECUDA;
+  if (h & 2) return FG_EDEVICE;
   return (h & 1) ? FG_ECAPACITY : FG_OK;
 }
 

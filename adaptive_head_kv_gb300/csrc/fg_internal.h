@@ -21,10 +21,20 @@ struct ProfileDims {
 cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
                                const int32_t* punct, int np, uint8_t* cls, cudaStream_t s);
 
-// Pass 1 (row log-sum-exp, base 2) and pass 2 (column and band sums), plain
-// SIMT fp32 arithmetic.
+// Row stride of the lse2 workspace: n rounded up to whole 128-row tiles.
+inline int lse_ld(int n) { return (n + 127) / 128 * 128; }
+
+// Pass 1 (row log-sum-exp, base 2; lse2 rows of stride ld) and pass 2
+// (column and band sums), plain SIMT fp32 arithmetic.
 cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                                float* colsum, float* bandcol, cudaStream_t s);
+                                int ld, float* colsum, float* bandcol, cudaStream_t s);
+
+// The same two passes on the tcgen05 tensor cores (bf16, d = 64 or 128).
+// A device-side wait that times out ORs 2 into *err.
+bool profile_tc_supported(const ProfileDims& pd);
+cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
+                              int ld, float* colsum, float* bandcol, int32_t* err,
+                              cudaStream_t s);
 
 // Top-k frequent set, candidate masses, policy, keep codes.
 cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,

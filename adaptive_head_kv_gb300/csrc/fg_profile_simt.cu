@@ -75,7 +75,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) lse_kernel(const T* __restrict__ Q,
                                                        const T* __restrict__ K,
                                                        float* __restrict__ lse2, int n,
-                                                       float sl2) {
+                                                       int ld, float sl2) {
   extern __shared__ float smem[];
   float* Qs = smem;
   float* Ks = smem + kTile * (D + 1);
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) lse_kernel(const T* __restrict__ Q,
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int i = i0 + ty * 4 + r;
-      if (i < n) lse2[(size_t)g * n + i] = m[r] + log2f(l[r]);
+      if (i < n) lse2[(size_t)g * ld + i] = m[r] + log2f(l[r]);
     }
   }
 }
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ 
                                                           const float* __restrict__ lse2,
                                                           float* __restrict__ colsum,
                                                           float* __restrict__ bandcol, int n,
-                                                          int w, float sl2) {
+                                                          int ld, int w, float sl2) {
   extern __shared__ float smem[];
   float* Ks = smem;
   float* Qs = smem + kTile * (D + 1);
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ 
   const int g = blockIdx.x, j0 = blockIdx.y * kTile;
   const T* Qg = Q + (size_t)g * n * D;
   const T* Kg = K + (size_t)g * n * D;
-  const float* Lg = lse2 + (size_t)g * n;
+  const float* Lg = lse2 + (size_t)g * ld;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   load_tile<T, D>(Ks, Kg, j0, n, 1.f);
   float cs[4] = {0.f, 0.f, 0.f, 0.f}, bs[4] = {0.f, 0.f, 0.f, 0.f};
@@ -179,8 +179,8 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ 
 }
 
 template <typename T, int D>
-cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2, float* colsum,
-                float* bandcol, cudaStream_t s) {
+cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2, int ld,
+                float* colsum, float* bandcol, cudaStream_t s) {
   const size_t sm1 = 2 * kTile * (D + 1) * sizeof(float);
   const size_t sm2 = sm1 + kTile * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(lse_kernel<T, D>,
@@ -190,21 +190,22 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2
                            (int)sm2);
   if (e != cudaSuccess) return e;
   dim3 grid(pd.G, cdiv(pd.n, kTile));
-  lse_kernel<T, D><<<grid, kThreads, sm1, s>>>((const T*)Q, (const T*)K, lse2, pd.n, pd.sl2);
+  lse_kernel<T, D><<<grid, kThreads, sm1, s>>>((const T*)Q, (const T*)K, lse2, pd.n, ld,
+                                               pd.sl2);
   colsum_kernel<T, D><<<grid, kThreads, sm2, s>>>((const T*)Q, (const T*)K, lse2, colsum,
-                                                  bandcol, pd.n, pd.w, pd.sl2);
+                                                  bandcol, pd.n, ld, pd.w, pd.sl2);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                                float* colsum, float* bandcol, cudaStream_t s) {
+                                int ld, float* colsum, float* bandcol, cudaStream_t s) {
   if (pd.dtype == FG_FP32)
-    return pd.d == 64 ? run<float, 64>(pd, Q, K, lse2, colsum, bandcol, s)
-                      : run<float, 128>(pd, Q, K, lse2, colsum, bandcol, s);
-  return pd.d == 64 ? run<__nv_bfloat16, 64>(pd, Q, K, lse2, colsum, bandcol, s)
-                    : run<__nv_bfloat16, 128>(pd, Q, K, lse2, colsum, bandcol, s);
+    return pd.d == 64 ? run<float, 64>(pd, Q, K, lse2, ld, colsum, bandcol, s)
+                      : run<float, 128>(pd, Q, K, lse2, ld, colsum, bandcol, s);
+  return pd.d == 64 ? run<__nv_bfloat16, 64>(pd, Q, K, lse2, ld, colsum, bandcol, s)
+                    : run<__nv_bfloat16, 128>(pd, Q, K, lse2, ld, colsum, bandcol, s);
 }
 
 }  // namespace fg

@@ -1,0 +1,342 @@
+// Prompt profiling on the tcgen05 tensor cores (bf16 Q/K, fp32 accumulate).
+//
+// FastGen profiles every head on A = softmax(s Q K^T) under the causal mask
+// (Model Tells You What to Discard, Method, eq. (C*)); the policies need, per
+// key j, colsum_j = sum_i A_ij and the band sum bandcol_j = sum_{j<=i<j+w} A_ij.
+// A is never written to memory.  Two passes over 128 x 128 score tiles:
+//   pass 1, query-major: CTA (g, query tile) streams its causal key tiles,
+//     S = Q_tile K_tile^T lands in tensor memory, the consumer warps keep the
+//     running row max and sum and write the base-2 row log-sum-exp;
+//   pass 2, key-major: CTA (g, key tile) streams query tiles i >= j,
+//     S^T = K_tile Q_tile^T, and each consumer thread owns one key (one TMEM
+//     lane), so its column and band sums accumulate in registers.
+// Warp roles per CTA: warps 0-3 consume TMEM (thread = tile row), warp 4
+// issues TMA loads (128-byte swizzled tiles, double-buffered), warp 5 issues
+// the MMAs (one thread) into two TMEM accumulators of 128 columns.
+// Every wait is bounded (about 1 s); on timeout the CTA records bit 1 in the
+// error word, lets its copies and MMAs land, frees tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fg_common.cuh"
+#include "fg_internal.h"
+#include "fg_sm100.cuh"
+
+namespace fg {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBlk = 128;       // tile rows and columns
+constexpr int kThreads = 192;   // 4 consumer warps + TMA warp + MMA warp
+constexpr int kStages = 2;      // streamed operand tiles in flight
+constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
+
+template <int D>
+struct TileCfg {
+  static constexpr int kHalves = D / 64;                       // 128-byte swizzle atoms per row
+  static constexpr uint32_t kHalfBytes = kBlk * 64 * 2;        // 16 KB
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kKSteps = D / 16;                       // MMAs of K = 16 per tile
+};
+
+template <int D>
+struct alignas(1024) TcSmem {
+  uint8_t a[TileCfg<D>::kTileBytes];             // loaded once: Q (pass 1) or K (pass 2)
+  uint8_t b[kStages][TileCfg<D>::kTileBytes];    // streamed: K (pass 1) or Q (pass 2)
+  uint64_t bar_a;
+  uint64_t bar_full[kStages], bar_empty[kStages];
+  uint64_t bar_sfull[2], bar_sempty[2];
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int row, int g) {
+#pragma unroll
+  for (int h = 0; h < TileCfg<D>::kHalves; ++h)
+    tma_load_3d(dst + h * TileCfg<D>::kHalfBytes, map, bar, h * 64, row, g);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_tile_mma(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlk, kBlk);
+#pragma unroll
+  for (int kk = 0; kk < TileCfg<D>::kKSteps; ++kk) {
+    const uint32_t off = (kk >> 2) * TileCfg<D>::kHalfBytes + (kk & 3) * 32;
+    umma_bf16(d_tmem, desc_kmajor_sw128(a_base + off), desc_kmajor_sw128(b_base + off), idesc,
+              kk > 0 ? 1u : 0u);
+  }
+}
+
+// PASS 1: lse2[g, i] (row stride ld) for the CTA's query tile.
+// PASS 2: colsum / bandcol for the CTA's key tile.
+template <int PASS, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    profile_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK, float* __restrict__ lse2,
+                      float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
+                      int ld, int nt, int w, float sl2, int32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem<D>& s = *reinterpret_cast<TcSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Longest tiles first: pass 1 starts with the last query tiles, pass 2
+  // with the first key tiles.
+  int g, at, b_first, nb;
+  if (PASS == 1) {
+    const int qt = nt - 1 - (int)(blockIdx.x / G);
+    g = blockIdx.x % G;
+    at = qt;
+    b_first = 0;
+    nb = qt + 1;
+  } else {
+    const int kt = blockIdx.x / G;
+    g = blockIdx.x % G;
+    at = kt;
+    b_first = kt;
+    nb = nt - kt;
+  }
+  const CUtensorMap* mapA = PASS == 1 ? &tmQ : &tmK;
+  const CUtensorMap* mapB = PASS == 1 ? &tmK : &tmQ;
+
+  if (warp == 0) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 128) {
+    mbar_init(&s.bar_a, 1);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.bar_full[i], 1);
+      mbar_init(&s.bar_empty[i], 1);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.bar_sfull[i], 1);
+      mbar_init(&s.bar_sempty[i], 4);
+    }
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  bool ok = true;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      mbar_expect_tx(&s.bar_a, TileCfg<D>::kTileBytes);
+      load_tile<D>(s.a, mapA, &s.bar_a, at * kBlk, g);
+      int issued = 0;
+      for (int t = 0; t < nb; ++t) {
+        const int st = t % kStages;
+        if (t >= kStages && !mbar_wait(&s.bar_empty[st], ((t / kStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&s.bar_full[st], TileCfg<D>::kTileBytes);
+        load_tile<D>(s.b[st], mapB, &s.bar_full[st], (b_first + t) * kBlk, g);
+        issued = t + 1;
+      }
+      if (!ok) {  // let every issued copy land before the CTA can exit
+        mbar_wait(&s.bar_a, 0);
+        for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+          mbar_wait(&s.bar_full[t % kStages], (t / kStages) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int issued = 0;
+      if (!mbar_wait(&s.bar_a, 0)) ok = false;
+      for (int t = 0; ok && t < nb; ++t) {
+        const int st = t % kStages, buf = t & 1;
+        if (!mbar_wait(&s.bar_full[st], (t / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        if (t >= 2 && !mbar_wait(&s.bar_sempty[buf], ((t >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_tile_mma<D>(tmem + buf * kBlk, smem_addr(s.a), smem_addr(s.b[st]));
+        umma_commit(&s.bar_sfull[buf]);
+        umma_commit(&s.bar_empty[st]);
+        issued = t + 1;
+      }
+      // the MMAs (and the arrivals they trigger) must complete before exit
+      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+        mbar_wait(&s.bar_empty[t % kStages], (t / kStages) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int row = threadIdx.x;  // TMEM lane = tile row
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m = FG_NEG_INF, l = 0.f;     // pass 1 state
+    float cs = 0.f, bs = 0.f;          // pass 2 state
+    const int self = at * kBlk + row;  // query (pass 1) or key (pass 2) position
+    for (int t = 0; t < nb; ++t) {
+      const int buf = t & 1;
+      const int other0 = (b_first + t) * kBlk;  // first key (pass 1) / query (pass 2) of the tile
+      if (!mbar_wait(&s.bar_sfull[buf], (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + buf * kBlk + c * 32, r[c]);
+      tmem_wait_ld(r[0]);
+      reg_barrier(r[1]);
+      reg_barrier(r[2]);
+      reg_barrier(r[3]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar_sempty[buf]);
+
+      if (PASS == 1) {
+        const bool edge = (t == nb - 1) || (other0 + kBlk > n);
+        float mx = FG_NEG_INF;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = other0 + c * 32 + e;
+            float v = __uint_as_float(r[c][e]);
+            if (edge && (j > self || j >= n)) v = FG_NEG_INF;
+            r[c][e] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        const float mnew = fmaxf(m, mx * sl2);
+        if (mnew != FG_NEG_INF) {
+          float sum = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sum += ex2(fmaf(__uint_as_float(r[c][e]), sl2, -mnew));
+          l = l * ex2(m - mnew) + sum;
+          m = mnew;
+        }
+      } else {
+        const float* lrow = lse2 + (size_t)g * ld + other0;
+        const bool diag = t == 0;
+        const bool band_all = other0 + kBlk - 1 < self + w;  // every column inside the band
+        const bool band_none = other0 >= self + w;           // no column inside it
+        float tsum = 0.f, bsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float lv[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(lrow + c * 32 + e));
+            lv[e] = x.x; lv[e + 1] = x.y; lv[e + 2] = x.z; lv[e + 3] = x.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            float p = ex2(fmaf(__uint_as_float(r[c][e]), sl2, -lv[e]));
+            if (diag && col < row) p = 0.f;  // query before the key: masked
+            tsum += p;
+            if (!band_all && !band_none && other0 + col < self + w) bsum += p;
+          }
+        }
+        cs += tsum;
+        bs += band_all ? tsum : (band_none ? 0.f : bsum);
+      }
+    }
+    if (ok) {
+      if (PASS == 1) {
+        // rows past the prompt get +inf so pass 2 reads them as zero mass
+        lse2[(size_t)g * ld + self] = self < n ? m + __log2f(l) : __int_as_float(0x7f800000);
+      } else if (self < n) {
+        colsum[(size_t)g * n + self] = cs;
+        bandcol[(size_t)g * n + self] = bs;
+      }
+    }
+  }
+  if (!ok) atomicOr(err, 2);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// [G, n, D] bf16 viewed as a 3-D tensor (D innermost); box 64 x 128 x 1 with
+// the 128-byte swizzle, out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, int G, int n, int D) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)n * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kBlk, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2, int ld,
+                float* colsum, float* bandcol, int32_t* err, cudaStream_t s) {
+  CUtensorMap tq, tk;
+  if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.G, pd.n, D))
+    return cudaErrorInvalidValue;
+  const int nt = cdiv(pd.n, kBlk);
+  const size_t smem = sizeof(TcSmem<D>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(profile_tc_kernel<1, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(profile_tc_kernel<2, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)pd.G * (unsigned)nt;
+  profile_tc_kernel<1, D><<<grid, kThreads, smem, s>>>(tq, tk, lse2, colsum, bandcol, pd.G, pd.n,
+                                                      ld, nt, pd.w, pd.sl2, err);
+  profile_tc_kernel<2, D><<<grid, kThreads, smem, s>>>(tq, tk, lse2, colsum, bandcol, pd.G, pd.n,
+                                                      ld, nt, pd.w, pd.sl2, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool profile_tc_supported(const ProfileDims& pd) {
+  return pd.dtype == FG_BF16 && (pd.d == 64 || pd.d == 128) &&
+         (long long)pd.G * cdiv(pd.n, kBlk) < (1LL << 31);
+}
+
+cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
+                              int ld, float* colsum, float* bandcol, int32_t* err,
+                              cudaStream_t s) {
+  return pd.d == 64 ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, err, s)
+                    : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, err, s);
+}
+
+}  // namespace fg

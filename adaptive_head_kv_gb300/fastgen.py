@@ -14,7 +14,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfastgen.so")
 
-FG_OK, FG_EINVAL, FG_EDTYPE, FG_EWORKSPACE, FG_ECAPACITY, FG_ECUDA = 0, -1, -2, -3, -4, -5
+FG_OK, FG_EINVAL, FG_EDTYPE, FG_EWORKSPACE, FG_ECAPACITY, FG_ECUDA, FG_EDEVICE = 0, -1, -2, -3, -4, -5, -6
 FG_BF16, FG_FP32 = 0, 1
 FG_POLICY_S, FG_POLICY_SP, FG_POLICY_SPF, FG_POLICY_SPFL, FG_POLICY_FULL = range(5)
 FG_KEEP_DROP, FG_KEEP_STATIC, FG_KEEP_WINDOW = 0, 1, 2
@@ -66,7 +66,7 @@ _SIGS = {
     "fastgen_version": (_I32, []),
     "fastgen_profile_workspace_bytes": (_SZ, [ctypes.POINTER(Params)]),
     "fastgen_profile": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, _I32, _P, _I32,
-                                       _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+                                       _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "fastgen_plan_bytes": (_SZ, [ctypes.POINTER(Params), _I32]),
     "fastgen_compact_plan": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _I32, _P, _SZ,
                                             ctypes.POINTER(PlanInfo), _P]),
@@ -143,13 +143,13 @@ def fastgen_profile_workspace_bytes(params: Params) -> int:
 
 
 def fastgen_profile(params, Q, K, token_ids, special_ids, punct_ids, policy, mass, cost, colsum,
-                    keep, kept, workspace, stream=None) -> None:
+                    keep, kept, workspace, dev_err, stream=None) -> None:
     ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     _check(lib().fastgen_profile(ctypes.byref(params), _ptr(Q), _ptr(K), _ptr(token_ids),
                                  _ptr(special_ids), _count(special_ids), _ptr(punct_ids),
                                  _count(punct_ids), _ptr(policy), _ptr(mass), _ptr(cost),
                                  _ptr(colsum), _ptr(keep), _ptr(kept), _ptr(workspace), ws_bytes,
-                                 _stream(stream)), "fastgen_profile")
+                                 _ptr(dev_err), _stream(stream)), "fastgen_profile")
 
 
 def fastgen_plan_bytes(params: Params, max_new_tokens: int) -> int:

@@ -49,7 +49,7 @@ class FastGenSession:
     def profile(self, Q, K, token_ids):
         fg.fastgen_profile(self.p, Q, K, token_ids, self.special, self.punct, self.policy,
                            self.mass, self.cost, self.colsum, self.keep, self.kept, self.ws,
-                           self.stream)
+                           self.dev_err, self.stream)
 
     def compact(self, K, V):
         self.info = fg.fastgen_compact_plan(self.p, self.policy, self.cost, self.max_new,
@@ -65,7 +65,6 @@ class FastGenSession:
             self.dws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
         fg.fastgen_compact(self.p, K, V, self.keep, self.plan, self.info, self.K_pool,
                            self.V_pool, self.pos_pool, self.stream)
-        self.dev_err.zero_()
 
     def prefill(self, Q, K, V, token_ids):
         self.profile(Q, K, token_ids)

@@ -46,7 +46,8 @@ typedef enum {
   FG_EDTYPE = -2,      /* dtype or head dim not supported */
   FG_EWORKSPACE = -3,  /* workspace / plan / pool buffer too small */
   FG_ECAPACITY = -4,   /* a head ran out of reserved cache rows while appending */
-  FG_ECUDA = -5        /* a CUDA runtime call or launch failed */
+  FG_ECUDA = -5,       /* a CUDA runtime call or launch failed */
+  FG_EDEVICE = -6      /* a kernel's bounded wait timed out (reported through dev_err) */
 } fg_status;
 
 typedef enum { FG_BF16 = 0, FG_FP32 = 1 } fg_dtype;
@@ -131,6 +132,11 @@ int32_t fastgen_version(void);
  *   policy [G] int8, mass [G,5] float, cost [G,5] int32, colsum [G,n] float,
  *   keep [G,n] uint8, kept [G] int32: outputs.
  *   workspace: >= fastgen_profile_workspace_bytes(p) bytes, 256-byte aligned.
+ *   dev_err: device int32 the call ORs with 2 if a kernel's bounded wait on
+ *            its own pipeline timed out (about 1 s); read with
+ *            fastgen_read_error (FG_EDEVICE).  Never set in normal operation.
+ * bf16 inputs run on the tcgen05 tensor cores (fp32 accumulation); fp32
+ * inputs on fp32 SIMT arithmetic.
  * Errors: FG_EINVAL for G, n < 1, T outside (0,1], ratios outside [0,1],
  * null/misaligned pointers; FG_EDTYPE for other d or dtype; FG_EWORKSPACE.
  * ------------------------------------------------------------------------ */
@@ -141,7 +147,7 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
                           int8_t* policy, float* mass, int32_t* cost, float* colsum,
                           uint8_t* keep, int32_t* kept, void* workspace,
-                          size_t workspace_bytes, void* stream);
+                          size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Compaction, step 1: the pool layout (Method: K_C, V_C = f(K, V, C)).
@@ -239,8 +245,9 @@ fg_status fastgen_decode_attn_noalloc(const fg_params* p, void* plan, const fg_p
                                       int32_t n_punct, int32_t pos, void* out,
                                       int32_t* dev_err, void* stream);
 
-/* Synchronously reads the device flag written by fastgen_decode_attn and
- * maps it to a status (FG_OK or FG_ECAPACITY).  Waits on `stream`. */
+/* Synchronously reads a device flag written by fastgen_profile or
+ * fastgen_decode_attn and maps it to a status (FG_OK, FG_ECAPACITY or
+ * FG_EDEVICE).  Waits on `stream`. */
 fg_status fastgen_read_error(const int32_t* dev_err, void* stream);
 
 #ifdef __cplusplus

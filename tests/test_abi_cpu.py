@@ -49,7 +49,7 @@ def test_struct_sizes():
 
 def test_status_strings_and_version():
     assert fg.status_string(0) == "ok"
-    for s in (-1, -2, -3, -4, -5):
+    for s in (-1, -2, -3, -4, -5, -6):
         assert fg.status_string(s) != "unknown status"
     assert fg.fastgen_version() >= 100
 
@@ -64,7 +64,7 @@ def test_workspace_sizes():
     p = P()
     G, n = 6, 100
     al = lambda x: (x + 255) // 256 * 256
-    assert fg.fastgen_profile_workspace_bytes(p) == 2 * al(G * n * 4) + al(n)
+    assert fg.fastgen_profile_workspace_bytes(p) == al(G * 128 * 4) + al(G * n * 4) + al(n)
     w = 30
     work = G * ((n + 7 + 255) // 256 + (w + 255) // 256)
     assert fg.fastgen_plan_bytes(p, 7) == al(G * 40) + 256 + work * 8
@@ -79,11 +79,11 @@ FAKE = 1 << 20  # an aligned address never dereferenced: checks fail first
 def profile_status(p, ws_bytes=1 << 40, ptrs=None, ns=1, np_=1):
     L = fg.lib()
     a = dict(Q=FAKE, K=FAKE, ids=FAKE, sp=FAKE, pu=FAKE, policy=FAKE, mass=FAKE, cost=FAKE,
-             colsum=FAKE, keep=FAKE, kept=FAKE, ws=FAKE)
+             colsum=FAKE, keep=FAKE, kept=FAKE, ws=FAKE, err=FAKE)
     a.update(ptrs or {})
     return L.fastgen_profile(ctypes.byref(p), a["Q"], a["K"], a["ids"], a["sp"], ns, a["pu"], np_,
                              a["policy"], a["mass"], a["cost"], a["colsum"], a["keep"],
-                             a["kept"], a["ws"], ws_bytes, None)
+                             a["kept"], a["ws"], ws_bytes, a["err"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -102,6 +102,7 @@ def test_profile_rejects_pointers_and_workspace():
     assert profile_status(p, ptrs=dict(K=FAKE + 8)) == fg.FG_EINVAL      # not 16-byte aligned
     assert profile_status(p, ptrs=dict(ws=FAKE + 16)) == fg.FG_EINVAL     # not 256-byte aligned
     assert profile_status(p, ptrs=dict(sp=None)) == fg.FG_EINVAL          # count 1, NULL set
+    assert profile_status(p, ptrs=dict(err=None)) == fg.FG_EINVAL
     assert profile_status(p, ns=-1) == fg.FG_EINVAL
     assert profile_status(p, np_=5000) == fg.FG_EINVAL
     assert profile_status(p, ws_bytes=fg.fastgen_profile_workspace_bytes(p) - 1) == fg.FG_EWORKSPACE
