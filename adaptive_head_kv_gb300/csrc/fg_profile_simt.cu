@@ -70,7 +70,7 @@ __device__ __forceinline__ float group16_sum(float v) {
   return v;
 }
 
-// Pass 1: lse2[g, i] = log2 sum_{j <= i} 2^(s log2e q_i.k_j).
+// Pass 1: lse2[g, i] = -log2 sum_{j <= i} 2^(s log2e q_i.k_j) (negated row LSE).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) lse_kernel(const T* __restrict__ Q,
                                                        const T* __restrict__ K,
@@ -122,12 +122,12 @@ __global__ void __launch_bounds__(kThreads) lse_kernel(const T* __restrict__ Q,
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int i = i0 + ty * 4 + r;
-      if (i < n) lse2[(size_t)g * ld + i] = m[r] + log2f(l[r]);
+      if (i < n) lse2[(size_t)g * ld + i] = -(m[r] + log2f(l[r]));
     }
   }
 }
 
-// Pass 2: colsum[g, j] = sum_{i >= j} 2^(s' - lse2_i), bandcol over i < j + w.
+// Pass 2: colsum[g, j] = sum_{i >= j} 2^(s'_ij + lse2_i), bandcol over i < j + w.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ Q,
                                                           const T* __restrict__ K,
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ 
       for (int c = 0; c < 4; ++c) {
         const int i = i0 + tx * 4 + c;
         if (i >= j && i < n) {
-          const float p = exp2f(s[r][c] - Ls[tx * 4 + c]);
+          const float p = exp2f(s[r][c] + Ls[tx * 4 + c]);
           cs[r] += p;
           if (i < j + w) bs[r] += p;
         }

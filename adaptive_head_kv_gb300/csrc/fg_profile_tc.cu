@@ -31,6 +31,7 @@ constexpr int kBlk = 128;       // tile rows and columns
 constexpr int kThreads = 192;   // 4 consumer warps + TMA warp + MMA warp
 constexpr int kStages = 2;      // streamed operand tiles in flight
 constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
+constexpr int kLseSlots = 4;    // pass 2: query-tile LSE vectors in flight
 
 template <int D>
 struct TileCfg {
@@ -44,17 +45,13 @@ template <int D>
 struct alignas(1024) TcSmem {
   uint8_t a[TileCfg<D>::kTileBytes];             // loaded once: Q (pass 1) or K (pass 2)
   uint8_t b[kStages][TileCfg<D>::kTileBytes];    // streamed: K (pass 1) or Q (pass 2)
+  float nlse[kLseSlots][kBlk];                   // pass 2: negated row LSEs of a query tile
   uint64_t bar_a;
   uint64_t bar_full[kStages], bar_empty[kStages];
   uint64_t bar_sfull[2], bar_sempty[2];
+  uint64_t bar_lfull[kLseSlots], bar_lempty[kLseSlots];
   uint32_t tmem_base;
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
@@ -75,12 +72,103 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t d_tmem, uint32_t a_base,
   }
 }
 
-// PASS 1: lse2[g, i] (row stride ld) for the CTA's query tile.
-// PASS 2: colsum / bandcol for the CTA's key tile.
+__device__ __forceinline__ float f(uint32_t u) { return __uint_as_float(u); }
+
+// Pass 1, one tile row of 128 scores: running max m and sum l in base 2.
+// `cut` masks columns c >= cut (causal diagonal and the prompt end); a
+// negative cut means no masking.
+__device__ __forceinline__ void lse_tile(uint32_t (&r)[4][32], float sl2, int cut, float& m,
+                                         float& l) {
+  if (cut >= 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (c * 32 + e >= cut) r[c][e] = __float_as_uint(FG_NEG_INF);
+  }
+  float mx[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    mx[c] = FG_NEG_INF;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) mx[c] = max3(mx[c], f(r[c][e]), f(r[c][e + 1]));
+  }
+  const float mnew = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+  if (mnew == FG_NEG_INF) return;
+  const uint64_t s2 = pack2(sl2, sl2), nm = pack2(-mnew, -mnew);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float x0, x1;
+      unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, nm), x0, x1);
+      acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pack2(ex2(x0), ex2(x1)));
+    }
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float a0, a1;
+    unpack2(acc[k], a0, a1);
+    sum += a0 + a1;
+  }
+  l = l * ex2(m - mnew) + sum;
+  m = mnew;
+}
+
+// Pass 2, one key row against 128 queries: adds sum_c A to cs and the part
+// inside the band to bs.  nl = negated base-2 row LSEs of the queries
+// (-inf past the prompt end).  lo: columns c < lo are before the key
+// (masked); band: columns c < band are inside the window.
+__device__ __forceinline__ void col_tile(const uint32_t (&r)[4][32], const float* nl, float sl2,
+                                         int lo, int band, float& cs, float& bs) {
+  const uint64_t s2 = pack2(sl2, sl2);
+  if (lo <= 0 && (band <= 0 || band >= kBlk)) {  // interior tile: no per-element test
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 L = *reinterpret_cast<const float4*>(nl + c * 32 + e);
+        float x0, x1, x2, x3;
+        unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
+        unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
+        acc[(e >> 2) & 3] = add2(acc[(e >> 2) & 3],
+                                 add2(pack2(ex2(x0), ex2(x1)), pack2(ex2(x2), ex2(x3))));
+      }
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a0, a1;
+      unpack2(acc[k], a0, a1);
+      t += a0 + a1;
+    }
+    cs += t;
+    if (band >= kBlk) bs += t;
+    return;
+  }
+  float ta[4] = {0.f, 0.f, 0.f, 0.f}, ba[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int col = c * 32 + e;
+      float p = ex2(fmaf(f(r[c][e]), sl2, nl[col]));
+      p = col < lo ? 0.f : p;
+      ta[e & 3] += p;
+      ba[e & 3] += col < band ? p : 0.f;
+    }
+  cs += (ta[0] + ta[1]) + (ta[2] + ta[3]);
+  bs += (ba[0] + ba[1]) + (ba[2] + ba[3]);
+}
+
+// PASS 1: nlse2[g, i] = -log2 sum_j 2^(s' q_i.k_j) (row stride ld) of the
+//         CTA's query tile; rows past the prompt get -inf.
+// PASS 2: colsum / bandcol of the CTA's key tile.
 template <int PASS, int D>
 __global__ void __launch_bounds__(kThreads, 2)
     profile_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmK, float* __restrict__ lse2,
+                      const __grid_constant__ CUtensorMap tmK, float* __restrict__ nlse2,
                       float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
                       int ld, int nt, int w, float sl2, int32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
@@ -88,21 +176,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Longest tiles first: pass 1 starts with the last query tiles, pass 2
-  // with the first key tiles.
-  int g, at, b_first, nb;
+  // Head-major order, so the tiles of one head run together and share its
+  // K (pass 1) or Q (pass 2) tiles through L2; longest tiles first in a head.
+  const int g = blockIdx.x / nt, tile = blockIdx.x % nt;
+  int at, b_first, nb;
   if (PASS == 1) {
-    const int qt = nt - 1 - (int)(blockIdx.x / G);
-    g = blockIdx.x % G;
-    at = qt;
+    at = nt - 1 - tile;
     b_first = 0;
-    nb = qt + 1;
+    nb = at + 1;
   } else {
-    const int kt = blockIdx.x / G;
-    g = blockIdx.x % G;
-    at = kt;
-    b_first = kt;
-    nb = nt - kt;
+    at = tile;
+    b_first = tile;
+    nb = nt - tile;
   }
   const CUtensorMap* mapA = PASS == 1 ? &tmQ : &tmK;
   const CUtensorMap* mapB = PASS == 1 ? &tmK : &tmQ;
@@ -123,6 +208,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&s.bar_sfull[i], 1);
       mbar_init(&s.bar_sempty[i], 4);
     }
+#pragma unroll
+    for (int i = 0; i < kLseSlots; ++i) {
+      mbar_init(&s.bar_lfull[i], 1);
+      mbar_init(&s.bar_lempty[i], 4);
+    }
     fence_barrier_init();
   }
   tc_fence_before();
@@ -136,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       mbar_expect_tx(&s.bar_a, TileCfg<D>::kTileBytes);
       load_tile<D>(s.a, mapA, &s.bar_a, at * kBlk, g);
-      int issued = 0;
+      int issued = 0, lissued = 0;
       for (int t = 0; t < nb; ++t) {
         const int st = t % kStages;
         if (t >= kStages && !mbar_wait(&s.bar_empty[st], ((t / kStages) - 1) & 1)) {
@@ -146,11 +236,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_expect_tx(&s.bar_full[st], TileCfg<D>::kTileBytes);
         load_tile<D>(s.b[st], mapB, &s.bar_full[st], (b_first + t) * kBlk, g);
         issued = t + 1;
+        if (PASS == 2) {
+          const int ls = t % kLseSlots;
+          if (t >= kLseSlots && !mbar_wait(&s.bar_lempty[ls], ((t / kLseSlots) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&s.bar_lfull[ls], kBlk * sizeof(float));
+          bulk_load(s.nlse[ls], nlse2 + (size_t)g * ld + (size_t)(b_first + t) * kBlk,
+                    kBlk * sizeof(float), &s.bar_lfull[ls]);
+          lissued = t + 1;
+        }
       }
       if (!ok) {  // let every issued copy land before the CTA can exit
         mbar_wait(&s.bar_a, 0);
         for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
           mbar_wait(&s.bar_full[t % kStages], (t / kStages) & 1);
+        for (int t = lissued > kLseSlots ? lissued - kLseSlots : 0; t < lissued; ++t)
+          mbar_wait(&s.bar_lfull[t % kLseSlots], (t / kLseSlots) & 1);
       }
     }
   } else if (warp == 5) {
@@ -205,59 +308,25 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) mbar_arrive(&s.bar_sempty[buf]);
 
       if (PASS == 1) {
-        const bool edge = (t == nb - 1) || (other0 + kBlk > n);
-        float mx = FG_NEG_INF;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = other0 + c * 32 + e;
-            float v = __uint_as_float(r[c][e]);
-            if (edge && (j > self || j >= n)) v = FG_NEG_INF;
-            r[c][e] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-        const float mnew = fmaxf(m, mx * sl2);
-        if (mnew != FG_NEG_INF) {
-          float sum = 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sum += ex2(fmaf(__uint_as_float(r[c][e]), sl2, -mnew));
-          l = l * ex2(m - mnew) + sum;
-          m = mnew;
-        }
+        // key columns j = other0 + c are valid for j <= self and j < n
+        const int lim = min(self + 1, n) - other0;
+        lse_tile(r, sl2, lim < kBlk ? max(lim, 0) : -1, m, l);
       } else {
-        const float* lrow = lse2 + (size_t)g * ld + other0;
-        const bool diag = t == 0;
-        const bool band_all = other0 + kBlk - 1 < self + w;  // every column inside the band
-        const bool band_none = other0 >= self + w;           // no column inside it
-        float tsum = 0.f, bsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float lv[32];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(lrow + c * 32 + e));
-            lv[e] = x.x; lv[e + 1] = x.y; lv[e + 2] = x.z; lv[e + 3] = x.w;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = c * 32 + e;
-            float p = ex2(fmaf(__uint_as_float(r[c][e]), sl2, -lv[e]));
-            if (diag && col < row) p = 0.f;  // query before the key: masked
-            tsum += p;
-            if (!band_all && !band_none && other0 + col < self + w) bsum += p;
-          }
+        const int ls = t % kLseSlots;
+        if (!mbar_wait(&s.bar_lfull[ls], (t / kLseSlots) & 1)) {
+          ok = false;
+          break;
         }
-        cs += tsum;
-        bs += band_all ? tsum : (band_none ? 0.f : bsum);
+        // query columns i = other0 + c count for i >= self (c >= self - other0)
+        // and lie in the window for i < self + w
+        col_tile(r, s.nlse[ls], sl2, self - other0, self + w - other0, cs, bs);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.bar_lempty[ls]);
       }
     }
     if (ok) {
       if (PASS == 1) {
-        // rows past the prompt get +inf so pass 2 reads them as zero mass
-        lse2[(size_t)g * ld + self] = self < n ? m + __log2f(l) : __int_as_float(0x7f800000);
+        nlse2[(size_t)g * ld + self] = self < n ? -(m + __log2f(l)) : FG_NEG_INF;
       } else if (self < n) {
         colsum[(size_t)g * n + self] = cs;
         bandcol[(size_t)g * n + self] = bs;
@@ -304,7 +373,7 @@ bool make_map(CUtensorMap* map, const void* base, int G, int n, int D) {
 }
 
 template <int D>
-cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2, int ld,
+cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse2, int ld,
                 float* colsum, float* bandcol, int32_t* err, cudaStream_t s) {
   CUtensorMap tq, tk;
   if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.G, pd.n, D))
@@ -318,9 +387,9 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2
                              (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)pd.G * (unsigned)nt;
-  profile_tc_kernel<1, D><<<grid, kThreads, smem, s>>>(tq, tk, lse2, colsum, bandcol, pd.G, pd.n,
+  profile_tc_kernel<1, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
                                                       ld, nt, pd.w, pd.sl2, err);
-  profile_tc_kernel<2, D><<<grid, kThreads, smem, s>>>(tq, tk, lse2, colsum, bandcol, pd.G, pd.n,
+  profile_tc_kernel<2, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
                                                       ld, nt, pd.w, pd.sl2, err);
   return cudaGetLastError();
 }
