@@ -28,7 +28,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kBlk = 128;       // tile rows and columns
-constexpr int kThreads = 192;   // 4 consumer warps + TMA warp + MMA warp
+constexpr int kConsumerWarps = 8;  // two per TMEM lane quarter, each taking 64 columns
+constexpr int kTmaWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kHalfCols = kBlk / 2;
 constexpr int kStages = 2;      // streamed operand tiles in flight
 constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
 constexpr int kLseSlots = 4;    // pass 2: query-tile LSE vectors in flight
@@ -46,6 +49,8 @@ struct alignas(1024) TcSmem {
   uint8_t a[TileCfg<D>::kTileBytes];             // loaded once: Q (pass 1) or K (pass 2)
   uint8_t b[kStages][TileCfg<D>::kTileBytes];    // streamed: K (pass 1) or Q (pass 2)
   float nlse[kLseSlots][kBlk];                   // pass 2: negated row LSEs of a query tile
+  float part[2][kBlk];                           // second-half partial results per row
+  int bad;                                       // some thread timed out
   uint64_t bar_a;
   uint64_t bar_full[kStages], bar_empty[kStages];
   uint64_t bar_sfull[2], bar_sempty[2];
@@ -74,31 +79,32 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t d_tmem, uint32_t a_base,
 
 __device__ __forceinline__ float f(uint32_t u) { return __uint_as_float(u); }
 
-// Pass 1, one tile row of 128 scores: running max m and sum l in base 2.
-// `cut` masks columns c >= cut (causal diagonal and the prompt end); a
-// negative cut means no masking.
-__device__ __forceinline__ void lse_tile(uint32_t (&r)[4][32], float sl2, int cut, float& m,
-                                         float& l) {
+// Pass 1, one thread's 64 scores of a tile row: running max m and sum l in
+// base 2.  Columns c >= cut (tile-relative, 0..127) are masked (causal
+// diagonal and the prompt end); cut < 0 means no masking.  c0 = first column.
+__device__ __forceinline__ void lse_tile(uint32_t (&r)[2][32], float sl2, int c0, int cut,
+                                         float& m, float& l) {
   if (cut >= 0) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int e = 0; e < 32; ++e)
-        if (c * 32 + e >= cut) r[c][e] = __float_as_uint(FG_NEG_INF);
+        if (c0 + c * 32 + e >= cut) r[c][e] = __float_as_uint(FG_NEG_INF);
   }
   float mx[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    mx[c] = FG_NEG_INF;
+  for (int k = 0; k < 4; ++k) {
+    const int c = k >> 1, e0 = (k & 1) * 16;
+    mx[k] = FG_NEG_INF;
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) mx[c] = max3(mx[c], f(r[c][e]), f(r[c][e + 1]));
+    for (int e = e0; e < e0 + 16; e += 2) mx[k] = max3(mx[k], f(r[c][e]), f(r[c][e + 1]));
   }
   const float mnew = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
   if (mnew == FG_NEG_INF) return;
   const uint64_t s2 = pack2(sl2, sl2), nm = pack2(-mnew, -mnew);
   uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
       float x0, x1;
@@ -116,20 +122,20 @@ __device__ __forceinline__ void lse_tile(uint32_t (&r)[4][32], float sl2, int cu
   m = mnew;
 }
 
-// Pass 2, one key row against 128 queries: adds sum_c A to cs and the part
-// inside the band to bs.  nl = negated base-2 row LSEs of the queries
-// (-inf past the prompt end).  lo: columns c < lo are before the key
-// (masked); band: columns c < band are inside the window.
-__device__ __forceinline__ void col_tile(const uint32_t (&r)[4][32], const float* nl, float sl2,
-                                         int lo, int band, float& cs, float& bs) {
+// Pass 2, one thread's 64 columns (starting at tile column c0) of a key row:
+// adds sum A to cs and the part inside the band to bs.  nl = negated base-2
+// LSEs of the tile's 128 queries (-inf past the prompt end).  Tile columns
+// c < lo precede the key (masked); columns c < band lie in the window.
+__device__ __forceinline__ void col_tile(const uint32_t (&r)[2][32], const float* nl, float sl2,
+                                         int c0, int lo, int band, float& cs, float& bs) {
   const uint64_t s2 = pack2(sl2, sl2);
-  if (lo <= 0 && (band <= 0 || band >= kBlk)) {  // interior tile: no per-element test
+  if (lo <= c0 && (band <= c0 || band >= c0 + kHalfCols)) {  // no per-element test
     uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        const float4 L = *reinterpret_cast<const float4*>(nl + c * 32 + e);
+        const float4 L = *reinterpret_cast<const float4*>(nl + c0 + c * 32 + e);
         float x0, x1, x2, x3;
         unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
         unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
@@ -144,15 +150,15 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[4][32], const float
       t += a0 + a1;
     }
     cs += t;
-    if (band >= kBlk) bs += t;
+    if (band >= c0 + kHalfCols) bs += t;
     return;
   }
   float ta[4] = {0.f, 0.f, 0.f, 0.f}, ba[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const int col = c * 32 + e;
+      const int col = c0 + c * 32 + e;
       float p = ex2(fmaf(f(r[c][e]), sl2, nl[col]));
       p = col < lo ? 0.f : p;
       ta[e & 3] += p;
@@ -196,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == kTmaWarp * 32) {
+    s.bad = 0;
     mbar_init(&s.bar_a, 1);
 #pragma unroll
     for (int i = 0; i < kStages; ++i) {
@@ -206,12 +213,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.bar_sfull[i], 1);
-      mbar_init(&s.bar_sempty[i], 4);
+      mbar_init(&s.bar_sempty[i], kConsumerWarps);
     }
 #pragma unroll
     for (int i = 0; i < kLseSlots; ++i) {
       mbar_init(&s.bar_lfull[i], 1);
-      mbar_init(&s.bar_lempty[i], 4);
+      mbar_init(&s.bar_lempty[i], kConsumerWarps);
     }
     fence_barrier_init();
   }
@@ -220,8 +227,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   bool ok = true;
+  float m = FG_NEG_INF, l = 0.f;  // pass 1 consumer state: running max and sum (base 2)
+  float cs = 0.f, bs = 0.f;       // pass 2 consumer state: column and band sums
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       mbar_expect_tx(&s.bar_a, TileCfg<D>::kTileBytes);
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           mbar_wait(&s.bar_lfull[t % kLseSlots], (t / kLseSlots) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       int issued = 0;
@@ -283,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int row = threadIdx.x;  // TMEM lane = tile row
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m = FG_NEG_INF, l = 0.f;     // pass 1 state
-    float cs = 0.f, bs = 0.f;          // pass 2 state
+    // warp w reads TMEM lanes 32*(w%4).. (its rows) and columns 64*(w/4)..
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = tile row
+    const int c0 = (warp >> 2) * kHalfCols;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0;
     const int self = at * kBlk + row;  // query (pass 1) or key (pass 2) position
     for (int t = 0; t < nb; ++t) {
       const int buf = t & 1;
@@ -296,13 +305,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + buf * kBlk + c * 32, r[c]);
+      uint32_t r[2][32];
+      tmem_ld32(lane_base + buf * kBlk, r[0]);
+      tmem_ld32(lane_base + buf * kBlk + 32, r[1]);
       tmem_wait_ld(r[0]);
       reg_barrier(r[1]);
-      reg_barrier(r[2]);
-      reg_barrier(r[3]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.bar_sempty[buf]);
@@ -310,32 +317,44 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (PASS == 1) {
         // key columns j = other0 + c are valid for j <= self and j < n
         const int lim = min(self + 1, n) - other0;
-        lse_tile(r, sl2, lim < kBlk ? max(lim, 0) : -1, m, l);
+        lse_tile(r, sl2, c0, lim < kBlk ? max(lim, 0) : -1, m, l);
       } else {
         const int ls = t % kLseSlots;
         if (!mbar_wait(&s.bar_lfull[ls], (t / kLseSlots) & 1)) {
           ok = false;
           break;
         }
-        // query columns i = other0 + c count for i >= self (c >= self - other0)
-        // and lie in the window for i < self + w
-        col_tile(r, s.nlse[ls], sl2, self - other0, self + w - other0, cs, bs);
+        // query columns i = other0 + c count for i >= self and lie in the
+        // window for i < self + w
+        col_tile(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.bar_lempty[ls]);
       }
     }
-    if (ok) {
-      if (PASS == 1) {
-        nlse2[(size_t)g * ld + self] = self < n ? -(m + __log2f(l)) : FG_NEG_INF;
-      } else if (self < n) {
-        colsum[(size_t)g * n + self] = cs;
-        bandcol[(size_t)g * n + self] = bs;
-      }
+    if (c0 != 0) {  // hand the second half's partial state to the first half
+      s.part[0][row] = PASS == 1 ? m : cs;
+      s.part[1][row] = PASS == 1 ? l : bs;
     }
   }
-  if (!ok) atomicOr(err, 2);
+  if (!ok) {
+    atomicOr(err, 2);
+    s.bad = 1;
+  }
   tc_fence_before();
   __syncthreads();
+  if (warp < 4 && !s.bad) {  // first-half threads merge the halves and write
+    const int row = warp * 32 + lane;
+    const int self = at * kBlk + row;
+    const float p0 = s.part[0][row], p1 = s.part[1][row];
+    if (PASS == 1) {
+      const float M = fmaxf(m, p0);
+      const float L = l * ex2(m - M) + p1 * ex2(p0 - M);
+      nlse2[(size_t)g * ld + self] = self < n ? -(M + __log2f(L)) : FG_NEG_INF;
+    } else if (self < n) {
+      colsum[(size_t)g * n + self] = cs + p0;
+      bandcol[(size_t)g * n + self] = bs + p1;
+    }
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
