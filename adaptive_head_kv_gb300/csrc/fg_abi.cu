@@ -88,7 +88,7 @@ size_t fastgen_profile_workspace_bytes(const fg_params* p) {
   if (check_params(p) != FG_OK) return 0;
   const size_t G = (size_t)p->B * p->L * p->H, n = p->n;
   return align_up(G * fg::lse_ld(p->n) * sizeof(float)) + align_up(G * n * sizeof(float)) +
-         align_up((size_t)p->B * n);
+         align_up((size_t)p->B * n) + kAlign;
 }
 
 fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
@@ -117,12 +117,14 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
   const size_t lse_bytes = align_up((size_t)pd.G * ld * sizeof(float));
   float* bandcol = (float*)(ws + lse_bytes);
   uint8_t* cls = (uint8_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)));
+  int32_t* sched = (int32_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)) +
+                              align_up((size_t)pd.B * pd.n));
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
                                          punct_ids, n_punct, cls, s);
   if (e == cudaSuccess) {
     if (fg::profile_tc_supported(pd))
-      e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, dev_err, s);
+      e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, sched, dev_err, s);
     else
       e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
   }

@@ -30,11 +30,12 @@ cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void
                                 int ld, float* colsum, float* bandcol, cudaStream_t s);
 
 // The same two passes on the tcgen05 tensor cores (bf16, d = 64 or 128).
-// A device-side wait that times out ORs 2 into *err.
+// sched: two ints of scratch (the passes' work counters).  A device-side
+// wait that times out ORs 2 into *err.
 bool profile_tc_supported(const ProfileDims& pd);
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                              int ld, float* colsum, float* bandcol, int32_t* err,
-                              cudaStream_t s);
+                              int ld, float* colsum, float* bandcol, int32_t* sched,
+                              int32_t* err, cudaStream_t s);
 
 // Top-k frequent set, candidate masses, policy, keep codes.
 cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,

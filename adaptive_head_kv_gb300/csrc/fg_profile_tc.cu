@@ -3,18 +3,24 @@
 // FastGen profiles every head on A = softmax(s Q K^T) under the causal mask
 // (Model Tells You What to Discard, Method, eq. (C*)); the policies need, per
 // key j, colsum_j = sum_i A_ij and the band sum bandcol_j = sum_{j<=i<j+w} A_ij.
-// A is never written to memory.  Two passes over 128 x 128 score tiles:
-//   pass 1, query-major: CTA (g, query tile) streams its causal key tiles,
+// A is never written to memory.  Two passes over 128 x 128 score tiles, each
+// a persistent kernel (two CTAs per SM) whose work units are claimed in
+// head-major order from a counter (the tiles of one head run together and
+// share its operands through L2; within a head the longest units go first):
+//   pass 1, query-major: unit (g, query tile) streams its causal key tiles,
 //     S = Q_tile K_tile^T lands in tensor memory, the consumer warps keep the
-//     running row max and sum and write the base-2 row log-sum-exp;
-//   pass 2, key-major: CTA (g, key tile) streams query tiles i >= j,
+//     running row max and sum and write the negated base-2 row log-sum-exp;
+//   pass 2, key-major: unit (g, key tile) streams query tiles i >= j,
 //     S^T = K_tile Q_tile^T, and each consumer thread owns one key (one TMEM
 //     lane), so its column and band sums accumulate in registers.
-// Warp roles per CTA: warps 0-3 consume TMEM (thread = tile row), warp 4
-// issues TMA loads (128-byte swizzled tiles, double-buffered), warp 5 issues
-// the MMAs (one thread) into two TMEM accumulators of 128 columns.
-// Every wait is bounded (about 1 s); on timeout the CTA records bit 1 in the
-// error word, lets its copies and MMAs land, frees tensor memory and exits.
+// Warp roles: warps 0-7 consume TMEM (two per lane quarter, 64 columns each),
+// warp 8 claims units and issues the TMA loads (128-byte swizzled tiles),
+// warp 9 issues the MMAs (one thread) into two 128-column accumulators.  All
+// pipeline state (stages, phases) carries over from unit to unit; tensor
+// memory is allocated once per CTA.
+// Every wait is bounded (about 1 s); a timeout sets an abort flag that ends
+// every other wait of the CTA at once, records bit 1 in the error word, and
+// the CTA lets its copies and MMAs land, frees tensor memory and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,19 +50,43 @@ struct TileCfg {
   static constexpr int kKSteps = D / 16;                       // MMAs of K = 16 per tile
 };
 
+struct UnitMeta {
+  int g, at, b_first, nb;  // head, own tile, first streamed tile, streamed tiles
+  int valid;               // 0 ends the stream
+};
+
 template <int D>
 struct alignas(1024) TcSmem {
-  uint8_t a[TileCfg<D>::kTileBytes];             // loaded once: Q (pass 1) or K (pass 2)
+  uint8_t a[TileCfg<D>::kTileBytes];             // per unit: Q (pass 1) or K (pass 2)
   uint8_t b[kStages][TileCfg<D>::kTileBytes];    // streamed: K (pass 1) or Q (pass 2)
   float nlse[kLseSlots][kBlk];                   // pass 2: negated row LSEs of a query tile
-  float part[2][kBlk];                           // second-half partial results per row
-  int bad;                                       // some thread timed out
-  uint64_t bar_a;
-  uint64_t bar_full[kStages], bar_empty[kStages];
-  uint64_t bar_sfull[2], bar_sempty[2];
-  uint64_t bar_lfull[kLseSlots], bar_lempty[kLseSlots];
+  float part[2][2][kBlk];                        // per unit parity: second-half partials
+  UnitMeta unit[2];
+  int abort;
+  uint64_t a_full, a_empty;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t sfull[2], sempty[2];
+  uint64_t lfull[kLseSlots], lempty[kLseSlots];
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t part_ready[2], part_done[2];
   uint32_t tmem_base;
 };
+
+// Bounded wait that returns at once once any thread of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!*abort) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return false;
+}
 
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
@@ -168,57 +198,52 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[2][32], const float
   bs += (ba[0] + ba[1]) + (ba[2] + ba[3]);
 }
 
-// PASS 1: nlse2[g, i] = -log2 sum_j 2^(s' q_i.k_j) (row stride ld) of the
-//         CTA's query tile; rows past the prompt get -inf.
-// PASS 2: colsum / bandcol of the CTA's key tile.
+// PASS 1: nlse2[g, i] = -log2 sum_j 2^(s' q_i.k_j) (row stride ld); rows past
+//         the prompt get -inf.
+// PASS 2: colsum / bandcol.
+// sched: this pass's unit counter (zero at launch).
 template <int PASS, int D>
 __global__ void __launch_bounds__(kThreads, 2)
     profile_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, float* __restrict__ nlse2,
                       float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
-                      int ld, int nt, int w, float sl2, int32_t* __restrict__ err) {
+                      int ld, int nt, int w, float sl2, int32_t* __restrict__ sched,
+                      int32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& s = *reinterpret_cast<TcSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // Head-major order, so the tiles of one head run together and share its
-  // K (pass 1) or Q (pass 2) tiles through L2; longest tiles first in a head.
-  const int g = blockIdx.x / nt, tile = blockIdx.x % nt;
-  int at, b_first, nb;
-  if (PASS == 1) {
-    at = nt - 1 - tile;
-    b_first = 0;
-    nb = at + 1;
-  } else {
-    at = tile;
-    b_first = tile;
-    nb = nt - tile;
-  }
+  volatile int* abort = &s.abort;
   const CUtensorMap* mapA = PASS == 1 ? &tmQ : &tmK;
   const CUtensorMap* mapB = PASS == 1 ? &tmK : &tmQ;
+  const int total_units = G * nt;
 
   if (warp == 0) {
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == kTmaWarp * 32) {
-    s.bad = 0;
-    mbar_init(&s.bar_a, 1);
+    s.abort = 0;
+    mbar_init(&s.a_full, 1);
+    mbar_init(&s.a_empty, 1);
 #pragma unroll
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.bar_full[i], 1);
-      mbar_init(&s.bar_empty[i], 1);
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.bar_sfull[i], 1);
-      mbar_init(&s.bar_sempty[i], kConsumerWarps);
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], kConsumerWarps);
+      mbar_init(&s.unit_full[i], 1);
+      mbar_init(&s.unit_empty[i], kConsumerWarps + 1);
+      mbar_init(&s.part_ready[i], kConsumerWarps / 2);
+      mbar_init(&s.part_done[i], kConsumerWarps / 2);
     }
 #pragma unroll
     for (int i = 0; i < kLseSlots; ++i) {
-      mbar_init(&s.bar_lfull[i], 1);
-      mbar_init(&s.bar_lempty[i], kConsumerWarps);
+      mbar_init(&s.lfull[i], 1);
+      mbar_init(&s.lempty[i], kConsumerWarps);
     }
     fence_barrier_init();
   }
@@ -226,69 +251,113 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  bool ok = true;
-  float m = FG_NEG_INF, l = 0.f;  // pass 1 consumer state: running max and sum (base 2)
-  float cs = 0.f, bs = 0.f;       // pass 2 consumer state: column and band sums
 
   if (warp == kTmaWarp) {
-    // ---------------------------------------------------------------- TMA
+    // ------------------------------------------------------- producer (TMA)
     if (lane == 0) {
-      mbar_expect_tx(&s.bar_a, TileCfg<D>::kTileBytes);
-      load_tile<D>(s.a, mapA, &s.bar_a, at * kBlk, g);
-      int issued = 0, lissued = 0;
-      for (int t = 0; t < nb; ++t) {
-        const int st = t % kStages;
-        if (t >= kStages && !mbar_wait(&s.bar_empty[st], ((t / kStages) - 1) & 1)) {
-          ok = false;
+      int bseq = 0, lseq = 0, ucount = 0;
+      int u = atomicAdd(sched, 1);
+      while (true) {
+        const int us = ucount & 1;
+        if (ucount >= 2 && !wait_or_abort(&s.unit_empty[us], ((ucount >> 1) - 1) & 1, abort))
+          break;
+        if (u >= total_units) {
+          s.unit[us].valid = 0;
+          mbar_arrive(&s.unit_full[us]);
           break;
         }
-        mbar_expect_tx(&s.bar_full[st], TileCfg<D>::kTileBytes);
-        load_tile<D>(s.b[st], mapB, &s.bar_full[st], (b_first + t) * kBlk, g);
-        issued = t + 1;
-        if (PASS == 2) {
-          const int ls = t % kLseSlots;
-          if (t >= kLseSlots && !mbar_wait(&s.bar_lempty[ls], ((t / kLseSlots) - 1) & 1)) {
-            ok = false;
+        const int g = u / nt, tile = u % nt;
+        UnitMeta um;
+        um.g = g;
+        um.valid = 1;
+        if (PASS == 1) {
+          um.at = nt - 1 - tile;
+          um.b_first = 0;
+          um.nb = um.at + 1;
+        } else {
+          um.at = tile;
+          um.b_first = tile;
+          um.nb = nt - tile;
+        }
+        s.unit[us] = um;
+        mbar_arrive(&s.unit_full[us]);
+        const int nxt = atomicAdd(sched, 1);  // claimed now, used after this unit
+        // the operand loaded per unit may be replaced once the previous
+        // unit's MMAs are done with it
+        if (ucount >= 1 && !wait_or_abort(&s.a_empty, (ucount - 1) & 1, abort)) break;
+        mbar_expect_tx(&s.a_full, TileCfg<D>::kTileBytes);
+        load_tile<D>(s.a, mapA, &s.a_full, um.at * kBlk, g);
+        bool stop = false;
+        for (int t = 0; t < um.nb; ++t) {
+          const int st = bseq % kStages;
+          if (bseq >= kStages && !wait_or_abort(&s.empty[st], ((bseq / kStages) - 1) & 1, abort)) {
+            stop = true;
             break;
           }
-          mbar_expect_tx(&s.bar_lfull[ls], kBlk * sizeof(float));
-          bulk_load(s.nlse[ls], nlse2 + (size_t)g * ld + (size_t)(b_first + t) * kBlk,
-                    kBlk * sizeof(float), &s.bar_lfull[ls]);
-          lissued = t + 1;
+          mbar_expect_tx(&s.full[st], TileCfg<D>::kTileBytes);
+          load_tile<D>(s.b[st], mapB, &s.full[st], (um.b_first + t) * kBlk, g);
+          ++bseq;
+          if (PASS == 2) {
+            const int ls = lseq % kLseSlots;
+            if (lseq >= kLseSlots &&
+                !wait_or_abort(&s.lempty[ls], ((lseq / kLseSlots) - 1) & 1, abort)) {
+              stop = true;
+              break;
+            }
+            mbar_expect_tx(&s.lfull[ls], kBlk * sizeof(float));
+            bulk_load(s.nlse[ls], nlse2 + (size_t)g * ld + (size_t)(um.b_first + t) * kBlk,
+                      kBlk * sizeof(float), &s.lfull[ls]);
+            ++lseq;
+          }
         }
+        if (stop) break;
+        ++ucount;
+        u = nxt;
       }
-      if (!ok) {  // let every issued copy land before the CTA can exit
-        mbar_wait(&s.bar_a, 0);
-        for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
-          mbar_wait(&s.bar_full[t % kStages], (t / kStages) & 1);
-        for (int t = lissued > kLseSlots ? lissued - kLseSlots : 0; t < lissued; ++t)
-          mbar_wait(&s.bar_lfull[t % kLseSlots], (t / kLseSlots) & 1);
+      if (*abort) {  // let the copies still in flight land before exiting
+        for (int q = bseq > kStages ? bseq - kStages : 0; q < bseq; ++q)
+          mbar_wait(&s.full[q % kStages], (q / kStages) & 1);
+        for (int q = lseq > kLseSlots ? lseq - kLseSlots : 0; q < lseq; ++q)
+          mbar_wait(&s.lfull[q % kLseSlots], (q / kLseSlots) & 1);
+        mbar_wait(&s.a_full, ucount & 1);
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
+    // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      int issued = 0;
-      if (!mbar_wait(&s.bar_a, 0)) ok = false;
-      for (int t = 0; ok && t < nb; ++t) {
-        const int st = t % kStages, buf = t & 1;
-        if (!mbar_wait(&s.bar_full[st], (t / kStages) & 1)) {
-          ok = false;
-          break;
+      int bseq = 0, sseq = 0, ucount = 0, acommits = 0;
+      while (true) {
+        const int us = ucount & 1;
+        if (!wait_or_abort(&s.unit_full[us], (ucount >> 1) & 1, abort)) break;
+        const UnitMeta um = s.unit[us];
+        mbar_arrive(&s.unit_empty[us]);
+        if (!um.valid) break;
+        if (!wait_or_abort(&s.a_full, ucount & 1, abort)) break;
+        bool stop = false;
+        for (int t = 0; t < um.nb; ++t) {
+          const int st = bseq % kStages, buf = sseq & 1;
+          if (!wait_or_abort(&s.full[st], (bseq / kStages) & 1, abort) ||
+              (sseq >= 2 && !wait_or_abort(&s.sempty[buf], ((sseq >> 1) - 1) & 1, abort))) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          issue_tile_mma<D>(tmem + buf * kBlk, smem_addr(s.a), smem_addr(s.b[st]));
+          umma_commit(&s.sfull[buf]);
+          umma_commit(&s.empty[st]);
+          ++bseq;
+          ++sseq;
         }
-        if (t >= 2 && !mbar_wait(&s.bar_sempty[buf], ((t >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_tile_mma<D>(tmem + buf * kBlk, smem_addr(s.a), smem_addr(s.b[st]));
-        umma_commit(&s.bar_sfull[buf]);
-        umma_commit(&s.bar_empty[st]);
-        issued = t + 1;
+        umma_commit(&s.a_empty);  // the unit's operand is free once these complete
+        ++acommits;
+        if (stop) break;
+        ++ucount;
       }
-      // the MMAs (and the arrivals they trigger) must complete before exit
-      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
-        mbar_wait(&s.bar_empty[t % kStages], (t / kStages) & 1);
+      // every MMA (and the arrivals it triggers) must complete before exit;
+      // the operand-release commit is the last one issued
+      for (int q = bseq > kStages ? bseq - kStages : 0; q < bseq; ++q)
+        mbar_wait(&s.empty[q % kStages], (q / kStages) & 1);
+      if (acommits > 0) mbar_wait(&s.a_empty, (acommits - 1) & 1);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -296,65 +365,83 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = tile row
     const int c0 = (warp >> 2) * kHalfCols;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0;
-    const int self = at * kBlk + row;  // query (pass 1) or key (pass 2) position
-    for (int t = 0; t < nb; ++t) {
-      const int buf = t & 1;
-      const int other0 = (b_first + t) * kBlk;  // first key (pass 1) / query (pass 2) of the tile
-      if (!mbar_wait(&s.bar_sfull[buf], (t >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t r[2][32];
-      tmem_ld32(lane_base + buf * kBlk, r[0]);
-      tmem_ld32(lane_base + buf * kBlk + 32, r[1]);
-      tmem_wait_ld(r[0]);
-      reg_barrier(r[1]);
-      tc_fence_before();
+    int sseq = 0, lseq = 0, ucount = 0;
+    while (true) {
+      const int us = ucount & 1;
+      if (!wait_or_abort(&s.unit_full[us], (ucount >> 1) & 1, abort)) break;
+      const UnitMeta um = s.unit[us];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.bar_sempty[buf]);
-
-      if (PASS == 1) {
-        // key columns j = other0 + c are valid for j <= self and j < n
-        const int lim = min(self + 1, n) - other0;
-        lse_tile(r, sl2, c0, lim < kBlk ? max(lim, 0) : -1, m, l);
-      } else {
-        const int ls = t % kLseSlots;
-        if (!mbar_wait(&s.bar_lfull[ls], (t / kLseSlots) & 1)) {
-          ok = false;
+      if (lane == 0) mbar_arrive(&s.unit_empty[us]);
+      if (!um.valid) break;
+      const int self = um.at * kBlk + row;  // query (pass 1) or key (pass 2) position
+      float m = FG_NEG_INF, l = 0.f;         // pass 1: running max and sum (base 2)
+      float cs = 0.f, bs = 0.f;              // pass 2: column and band sums
+      bool stop = false;
+      for (int t = 0; t < um.nb; ++t) {
+        const int buf = sseq & 1;
+        const int other0 = (um.b_first + t) * kBlk;  // first key / query of the tile
+        if (!wait_or_abort(&s.sfull[buf], (sseq >> 1) & 1, abort)) {
+          stop = true;
           break;
         }
-        // query columns i = other0 + c count for i >= self and lie in the
-        // window for i < self + w
-        col_tile(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
+        tc_fence_after();
+        uint32_t r[2][32];
+        tmem_ld32(lane_base + buf * kBlk, r[0]);
+        tmem_ld32(lane_base + buf * kBlk + 32, r[1]);
+        tmem_wait_ld(r[0]);
+        reg_barrier(r[1]);
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.bar_lempty[ls]);
+        if (lane == 0) mbar_arrive(&s.sempty[buf]);
+        ++sseq;
+        if (PASS == 1) {
+          // key columns j = other0 + c are valid for j <= self and j < n
+          const int lim = min(self + 1, n) - other0;
+          lse_tile(r, sl2, c0, lim < kBlk ? max(lim, 0) : -1, m, l);
+        } else {
+          const int ls = lseq % kLseSlots;
+          if (!wait_or_abort(&s.lfull[ls], (lseq / kLseSlots) & 1, abort)) {
+            stop = true;
+            break;
+          }
+          // query columns i = other0 + c count for i >= self and lie in the
+          // window for i < self + w
+          col_tile(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.lempty[ls]);
+          ++lseq;
+        }
       }
+      if (stop) break;
+      // merge the two column halves of every row: the second half hands over
+      const int ps = ucount & 1;
+      if (c0 != 0) {
+        if (ucount >= 2 && !wait_or_abort(&s.part_done[ps], ((ucount >> 1) - 1) & 1, abort))
+          break;
+        s.part[ps][0][row] = PASS == 1 ? m : cs;
+        s.part[ps][1][row] = PASS == 1 ? l : bs;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.part_ready[ps]);
+      } else {
+        if (!wait_or_abort(&s.part_ready[ps], (ucount >> 1) & 1, abort)) break;
+        const float p0 = s.part[ps][0][row], p1 = s.part[ps][1][row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.part_done[ps]);
+        if (PASS == 1) {
+          const float M = fmaxf(m, p0);
+          const float L = l * ex2(m - M) + p1 * ex2(p0 - M);
+          nlse2[(size_t)um.g * ld + self] = self < n ? -(M + __log2f(L)) : FG_NEG_INF;
+        } else if (self < n) {
+          colsum[(size_t)um.g * n + self] = cs + p0;
+          bandcol[(size_t)um.g * n + self] = bs + p1;
+        }
+      }
+      ++ucount;
     }
-    if (c0 != 0) {  // hand the second half's partial state to the first half
-      s.part[0][row] = PASS == 1 ? m : cs;
-      s.part[1][row] = PASS == 1 ? l : bs;
-    }
-  }
-  if (!ok) {
-    atomicOr(err, 2);
-    s.bad = 1;
   }
   tc_fence_before();
   __syncthreads();
-  if (warp < 4 && !s.bad) {  // first-half threads merge the halves and write
-    const int row = warp * 32 + lane;
-    const int self = at * kBlk + row;
-    const float p0 = s.part[0][row], p1 = s.part[1][row];
-    if (PASS == 1) {
-      const float M = fmaxf(m, p0);
-      const float L = l * ex2(m - M) + p1 * ex2(p0 - M);
-      nlse2[(size_t)g * ld + self] = self < n ? -(M + __log2f(L)) : FG_NEG_INF;
-    } else if (self < n) {
-      colsum[(size_t)g * n + self] = cs + p0;
-      bandcol[(size_t)g * n + self] = bs + p1;
-    }
-  }
+  if (threadIdx.x == 0 && s.abort) atomicOr(err, 2);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -391,9 +478,21 @@ bool make_map(CUtensorMap* map, const void* base, int G, int n, int D) {
          CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
 template <int D>
 cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse2, int ld,
-                float* colsum, float* bandcol, int32_t* err, cudaStream_t s) {
+                float* colsum, float* bandcol, int32_t* sched, int32_t* err, cudaStream_t s) {
   CUtensorMap tq, tk;
   if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.G, pd.n, D))
     return cudaErrorInvalidValue;
@@ -405,11 +504,16 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
     e = cudaFuncSetAttribute(profile_tc_kernel<2, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)pd.G * (unsigned)nt;
+  const long long units = (long long)pd.G * nt;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = (unsigned)(units < 2LL * sms ? units : 2LL * sms);
+  e = cudaMemsetAsync(sched, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
   profile_tc_kernel<1, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
-                                                      ld, nt, pd.w, pd.sl2, err);
+                                                      ld, nt, pd.w, pd.sl2, sched, err);
   profile_tc_kernel<2, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
-                                                      ld, nt, pd.w, pd.sl2, err);
+                                                      ld, nt, pd.w, pd.sl2, sched + 1, err);
   return cudaGetLastError();
 }
 
@@ -421,10 +525,10 @@ bool profile_tc_supported(const ProfileDims& pd) {
 }
 
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                              int ld, float* colsum, float* bandcol, int32_t* err,
-                              cudaStream_t s) {
-  return pd.d == 64 ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, err, s)
-                    : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, err, s);
+                              int ld, float* colsum, float* bandcol, int32_t* sched,
+                              int32_t* err, cudaStream_t s) {
+  return pd.d == 64 ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, sched, err, s)
+                    : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, sched, err, s);
 }
 
 }  // namespace fg

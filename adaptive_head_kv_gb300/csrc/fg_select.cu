@@ -18,7 +18,7 @@
 namespace fg {
 namespace {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 
 __global__ void token_class_kernel(const int32_t* __restrict__ ids, int count,
                                    const int32_t* __restrict__ special, int ns,
@@ -51,23 +51,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     int8_t* __restrict__ policy, float* __restrict__ mass, int32_t* __restrict__ cost,
     uint8_t* __restrict__ keep, int32_t* __restrict__ kept) {
   __shared__ unsigned hist[256];
-  __shared__ unsigned s_prefix;
-  __shared__ int s_krem;
+  __shared__ int s_bin, s_krem, s_eq;
   __shared__ int scan_scratch[33];
   __shared__ double dred[32];
   __shared__ int ired[32];
   __shared__ int s_policy;
 
   const int g = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* c = colsum + (size_t)g * n;
   const float* bc = bandcol + (size_t)g * n;
   const uint8_t* cl = cls + (size_t)(g / HL) * n;
   uint8_t* kp = keep + (size_t)g * n;
   const bool partial = k > 0 && k < n;
 
-  // --- 1. radix select of the k-th largest colsum ---------------------------
+  // --- 1. radix select of the k-th largest colsum (8-bit digits, MSB first)
   unsigned prefix = 0, mask = 0;
-  int krem = k;
+  int krem = k, eq_count = 0;
   if (partial) {
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
@@ -77,25 +77,45 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int acc = 0, bin = 255;
-        for (; bin > 0; --bin) {
-          if (acc + (int)hist[bin] >= krem) break;
-          acc += hist[bin];
+      if (warp == 0) {
+        // lane l owns bins 255-8l .. 248-8l, scanned from the top down
+        unsigned h[8], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          h[i] = hist[255 - 8 * lane - i];
+          tot += h[i];
         }
-        s_krem = krem - acc;
-        s_prefix = prefix | ((unsigned)bin << shift);
+        unsigned incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= (unsigned)krem);
+        const int L = hit ? __ffs(hit) - 1 : 31;
+        if (lane == L) {
+          unsigned acc = incl - tot;
+          int i = 0;
+          for (; i < 7; ++i) {
+            if (acc + h[i] >= (unsigned)krem) break;
+            acc += h[i];
+          }
+          s_bin = 255 - 8 * lane - i;
+          s_krem = krem - (int)acc;
+          s_eq = (int)h[i];
+        }
       }
       __syncthreads();
-      krem = s_krem;
-      prefix = s_prefix;
+      prefix |= (unsigned)s_bin << shift;
       mask |= 255u << shift;
-      __syncthreads();
+      krem = s_krem;
+      eq_count = s_eq;  // after the last digit: values equal to the threshold
     }
   }
   // Selected: value above the threshold, or equal to it and among the first
-  // `krem` equal values in index order.
+  // `krem` equal values in index order (all of them when krem covers them).
   const unsigned thr = prefix;
+  const bool rank_ties = partial && krem < eq_count;
 
   // --- 2. masses and costs --------------------------------------------------
   double a0 = 0, a1 = 0, a2 = 0, a3 = 0;
@@ -107,14 +127,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const float cj = valid ? c[j] : 0.f;
     const unsigned u = __float_as_uint(cj);
     const int is_eq = (valid && partial && u == thr) ? 1 : 0;
-    int eq_total;
-    const int eq_rank = eq_seen + block_exclusive_scan(is_eq, scan_scratch, &eq_total);
-    eq_seen += eq_total;
+    int eq_rank = 0;
+    if (rank_ties) {  // block-uniform branch
+      int eq_total;
+      eq_rank = eq_seen + block_exclusive_scan(is_eq, scan_scratch, &eq_total);
+      eq_seen += eq_total;
+    }
     if (!valid) continue;
     bool in_f;
     if (k >= n) in_f = true;
     else if (k == 0) in_f = false;
-    else in_f = (u > thr) || (is_eq && eq_rank < krem);
+    else in_f = (u > thr) || (is_eq && (!rank_ties || eq_rank < krem));
     const uint8_t t = cl[j];
     const bool s0 = t & 1, s1 = t != 0, s2 = s1 || in_f, win = j >= n - w;
     const float bj = bc[j];

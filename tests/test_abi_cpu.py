@@ -64,7 +64,7 @@ def test_workspace_sizes():
     p = P()
     G, n = 6, 100
     al = lambda x: (x + 255) // 256 * 256
-    assert fg.fastgen_profile_workspace_bytes(p) == al(G * 128 * 4) + al(G * n * 4) + al(n)
+    assert fg.fastgen_profile_workspace_bytes(p) == al(G * 128 * 4) + al(G * n * 4) + al(n) + 256
     w = 30
     work = G * ((n + 7 + 255) // 256 + (w + 255) // 256)
     assert fg.fastgen_plan_bytes(p, 7) == al(G * 40) + 256 + work * 8
