@@ -338,11 +338,9 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     r = run_ours(args, cfg, rank, world)
-    mine = torch.tensor([r["step_ms"], r["prof_ms"] + r["comp_ms"], r["decode_ms"],
-                         r["dec_ms"].mean()], dtype=torch.float64, device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(mine, op=torch.distributed.ReduceOp.MAX)
-    step_ms, prompt_ms, decode_ms, dec_launch_ms = mine.tolist()
+    step_ms, prompt_ms, decode_ms, dec_launch_ms = reduce_max(
+        [r["step_ms"], r["prof_ms"] + r["comp_ms"], r["decode_ms"], r["dec_ms"].mean()], world,
+        "cuda")
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
@@ -401,29 +399,33 @@ def fg_launches(call):
 
 def run_reference(args, cfg, world):
     """The oracle timed as it stands on the host cores, on bounded samples of
-    the same workload, reported in the same metric."""
+    the same workload, reported in the same metric (extrapolated linearly in
+    heads: every head of a configuration costs the same)."""
     heads_per_step = 2
     rng = np.random.default_rng(7)
-    for _ in range(args.warmup):
-        pass  # the oracle has nothing to warm up; warm-up steps are not timed
+    for _ in range(args.warmup):  # untimed: one head each
+        oracle_sample(cfg, [int(rng.integers(cfg.G))])
     t_pc = t_dec = 0.0
     sampled = 0
+    t0 = time.perf_counter()
     for _ in range(args.steps):
         heads = sorted(rng.choice(cfg.G, size=heads_per_step, replace=False).tolist())
         a, b = oracle_sample(cfg, heads)
         t_pc += a
         t_dec += b
         sampled += heads_per_step
+    wall_ms = (time.perf_counter() - t0) * 1e3 / max(args.steps, 1)
     scale = cfg.G / sampled
-    value = cfg.B * cfg.n / (t_pc * scale) * 1.0
-    step_ms = (t_pc + t_dec) * scale / args.steps * 1e3
+    value = cfg.B * cfg.n / (t_pc * scale)
     cores = host_threads()
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
-           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall_ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded generator)",
            "config": {"workload": f"{cfg.name}", "G": cfg.G,
-                      "step": f"{heads_per_step} sampled heads, extrapolated to all {cfg.G}"},
+                      "step": f"{heads_per_step} sampled heads (profile+compact+{cfg.steps} "
+                              f"decode steps each); value extrapolated to all {cfg.G} heads"},
+           "extrapolated_ms_per_full_step": (t_pc + t_dec) * scale / max(args.steps, 1) * 1e3,
            "decode_tok_s": cfg.B * cfg.steps / (t_dec * scale),
            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
                             "sample": f"{heads_per_step} heads per step x {args.steps} steps of "
@@ -431,6 +433,16 @@ def run_reference(args, cfg, world):
            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def reduce_max(values, world, device):
+    """Element-wise maximum of per-rank timings (the only cross-rank step)."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
 
 
 if __name__ == "__main__":
