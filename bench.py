@@ -30,6 +30,74 @@ sys.path.insert(0, ROOT)
 METRIC = "profile+compact prompt tok/s; compressed-cache decode tok/s and HBM GB/s"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+_CSRC = os.path.join("adaptive_head_kv_gb300", "csrc")
+# the kernels behind each roofline entry, and the sources that define them
+KERNEL_GROUPS = {
+    "decode": dict(patterns=("split_kernel", "combine_kernel"), calls="split_kernel",
+                   sources=("fg_decode.cu", "fg_common.cuh", "fg_internal.h")),
+    "profile": dict(patterns=("profile_tc_kernel", "select_kernel", "token_class_kernel"),
+                    calls="select_kernel",
+                    sources=("fg_profile_tc.cu", "fg_sm100.cuh", "fg_select.cu", "fg_common.cuh",
+                             "fg_internal.h")),
+}
+
+
+def source_digest(group):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_GROUPS[group]["sources"]:
+        with open(os.path.join(ROOT, _CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def record_traffic(csv_path, workload, command):
+    """Writes DRAM bytes per call of each kernel group from an ncu CSV (metrics
+    dram__bytes_read.sum and dram__bytes_write.sum), tagged with the sources'
+    digest so that a later kernel change voids the figure."""
+    import csv
+
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    h = rows[hi]
+    ki, mi, vi, ui = (h.index(x) for x in ("Kernel Name", "Metric Name", "Metric Value",
+                                            "Metric Unit"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    out = {}
+    for group, spec in KERNEL_GROUPS.items():
+        total, calls = 0.0, 0
+        for r in rows[hi + 1:]:
+            if len(r) != len(h) or not any(p in r[ki] for p in spec["patterns"]):
+                continue
+            if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                total += float(r[vi].replace(",", "")) * scale[r[ui]]
+            if r[mi] == "dram__bytes_read.sum" and spec["calls"] in r[ki]:
+                calls += 1
+        if calls:
+            out[group] = {"bytes_per_call": total / calls, "calls": calls,
+                          "workload": workload, "source_sha256": source_digest(group),
+                          "command": command}
+    os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out, indent=1))
+
+
+def load_traffic(group, workload):
+    """Measured DRAM bytes per call, or None if absent, taken on another
+    workload, or taken on kernels that have changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[group]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256") != source_digest(group):
+        return None
+    return rec["bytes_per_call"]
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -319,6 +387,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (smaller cases for profiler captures)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="write profiles/traffic.json from an ncu CSV of DRAM byte counters")
+    ap.add_argument("--traffic-command", default="",
+                    help="the command that produced the CSV (stored with the figures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -327,6 +399,9 @@ def main():
     cfg = CONFIGS[args.config]
     if args.layers:
         cfg = cfg.with_(L=args.layers, name=f"{cfg.name}_L{args.layers}")
+    if args.record_traffic:
+        record_traffic(args.record_traffic, cfg.name, args.traffic_command)
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -351,12 +426,12 @@ def main():
     prof_ach = r["prof_flops"] / (r["prof_ms"] * 1e-3) / 1e12
     dec_roof = {"kernel": "fastgen_decode_attn (split + combine)", "bound": "hbm",
                 "achieved": dec_ach, "peak": pk["hbm"], "unit": "GB/s", "frac": dec_ach / pk["hbm"],
-                "traffic": None, "peak_source": pk["src"],
+                "traffic": load_traffic("decode", cfg.name), "peak_source": pk["src"],
                 "algorithmic_bytes_per_launch": r["dec_bytes"]}
-    prof_roof = {"kernel": "fastgen_profile (both passes + select)", "bound": "tensor",
-                 "achieved": prof_ach, "peak": pk["bf16"], "unit": "TFLOP/s",
-                 "frac": prof_ach / pk["bf16"], "traffic": None, "peak_source": pk["src"],
-                 "algorithmic_flops_per_launch": r["prof_flops"]}
+    prof_roof = {"kernel": "fastgen_profile (token classes, both passes, select)",
+                 "bound": "tensor", "achieved": prof_ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                 "frac": prof_ach / pk["bf16"], "traffic": load_traffic("profile", cfg.name),
+                 "peak_source": pk["src"], "algorithmic_flops_per_launch": r["prof_flops"]}
     dec_total = r["decode_ms"]
     dominant, other = (dec_roof, prof_roof) if dec_total >= r["prof_ms"] else (prof_roof, dec_roof)
     e = r["e2e"]
