@@ -17,31 +17,41 @@ def make_params(B, L, H, n, d, dtype, T, r_l, r_f, scale=0.0) -> fg.Params:
     return fg.Params(B, L, H, n, d, code, T, r_l, r_f, scale)
 
 
+GUARD_BYTES = 4096
+GUARD_FILL = 0x5A
+
+
 class FastGenSession:
+    """Owns the buffers of one batch of heads.  With guard=True every buffer
+    the library writes gets GUARD_BYTES of canary bytes on both sides, and
+    check_guards() reports any that changed (a bounds check for tests)."""
+
     def __init__(self, params: fg.Params, special_ids, punct_ids, max_new_tokens: int,
-                 device="cuda", stream=None):
+                 device="cuda", stream=None, guard=False):
         self.p = params
         self.device = torch.device(device)
         self.stream = stream
         self.max_new = int(max_new_tokens)
+        self.guard = guard
+        self._guards = []
         G, n = params.B * params.L * params.H, params.n
         self.G = G
         self.tdtype = torch.bfloat16 if params.dtype == fg.FG_BF16 else torch.float32
         dev = self.device
         self.special = torch.as_tensor(special_ids, dtype=torch.int32, device=dev)
         self.punct = torch.as_tensor(punct_ids, dtype=torch.int32, device=dev)
-        self.policy = torch.empty(G, dtype=torch.int8, device=dev)
-        self.mass = torch.empty(G, 5, dtype=torch.float32, device=dev)
-        self.cost = torch.empty(G, 5, dtype=torch.int32, device=dev)
-        self.colsum = torch.empty(G, n, dtype=torch.float32, device=dev)
-        self.keep = torch.empty(G, n, dtype=torch.uint8, device=dev)
-        self.kept = torch.empty(G, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(fg.fastgen_profile_workspace_bytes(params), dtype=torch.uint8,
-                              device=dev)
-        self.plan = torch.empty(fg.fastgen_plan_bytes(params, self.max_new), dtype=torch.uint8,
-                                device=dev)
-        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.out = torch.empty(G, params.d, dtype=self.tdtype, device=dev)
+        E = self._empty
+        self.policy = E((G,), torch.int8)
+        self.mass = E((G, 5), torch.float32)
+        self.cost = E((G, 5), torch.int32)
+        self.colsum = E((G, n), torch.float32)
+        self.keep = E((G, n), torch.uint8)
+        self.kept = E((G,), torch.int32)
+        self.ws = E((fg.fastgen_profile_workspace_bytes(params),), torch.uint8)
+        self.plan = E((fg.fastgen_plan_bytes(params, self.max_new),), torch.uint8)
+        self.dev_err = E((1,), torch.int32)
+        self.dev_err.zero_()
+        self.out = E((G, params.d), self.tdtype)
         self.info = None
         self.K_pool = self.V_pool = self.pos_pool = None
         self.dws = None
@@ -57,12 +67,12 @@ class FastGenSession:
         rows = int(self.info.pool_rows)
         if self.pos_pool is None or self.pos_pool.numel() < rows:
             d = self.p.d
-            self.K_pool = torch.empty(rows, d, dtype=self.tdtype, device=self.device)
-            self.V_pool = torch.empty(rows, d, dtype=self.tdtype, device=self.device)
-            self.pos_pool = torch.empty(rows, dtype=torch.int32, device=self.device)
+            self.K_pool = self._empty((rows, d), self.tdtype)
+            self.V_pool = self._empty((rows, d), self.tdtype)
+            self.pos_pool = self._empty((rows,), torch.int32)
         need = fg.fastgen_decode_workspace_bytes(self.p, self.info)
         if self.dws is None or self.dws.numel() < need:
-            self.dws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            self.dws = self._empty((max(need, 256),), torch.uint8)
         fg.fastgen_compact(self.p, K, V, self.keep, self.plan, self.info, self.K_pool,
                            self.V_pool, self.pos_pool, self.stream)
 
@@ -76,6 +86,27 @@ class FastGenSession:
                                self.pos_pool, q, k_new, v_new, new_ids, self.special, self.punct,
                                pos, out, self.dws, self.dev_err, self.stream)
         return out
+
+    def _empty(self, shape, dtype):
+        if not self.guard:
+            return torch.empty(shape, dtype=dtype, device=self.device)
+        nbytes = int(torch.Size(shape).numel()) * torch.empty((), dtype=dtype).element_size()
+        body = (nbytes + 255) // 256 * 256
+        raw = torch.full((GUARD_BYTES + body + GUARD_BYTES,), GUARD_FILL, dtype=torch.uint8,
+                         device=self.device)
+        view = raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(shape)
+        self._guards.append((raw, body))
+        return view
+
+    def check_guards(self):
+        """Number of guard buffers whose canaries changed (0 when none did)."""
+        bad = 0
+        for raw, body in self._guards:
+            lo = raw[:GUARD_BYTES]
+            hi = raw[GUARD_BYTES + body:]
+            if bool((lo != GUARD_FILL).any()) or bool((hi != GUARD_FILL).any()):
+                bad += 1
+        return bad
 
     def descriptors(self):
         """Host copy of the per-head descriptors (for inspection and tests)."""

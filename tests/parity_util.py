@@ -31,8 +31,9 @@ def dec_atol(dtype: str) -> float:
     return 2e-2 if dtype == "bf16" else 1e-5
 
 
-def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True):
-    """Whole path on the GPU.  Returns host copies of everything compared."""
+def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True, guard=True):
+    """Whole path on the GPU.  Returns host copies of everything compared.
+    Every buffer the library writes is guarded by canaries (see session)."""
     from adaptive_head_kv_gb300.session import FastGenSession, make_params
 
     w = make_workload(cfg, seed)
@@ -45,7 +46,7 @@ def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True):
     T = cfg.T if T is None else T
     p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, T, cfg.r_l, cfg.r_f)
     s = FastGenSession(p, special_ids(seed), punct_ids(seed),
-                       cfg.steps if max_new is None else max_new)
+                       cfg.steps if max_new is None else max_new, guard=guard)
     s.prefill(Q, K, V, ids[:, :n].contiguous())
     torch.cuda.synchronize()
     res = dict(workload=w, policy=s.policy.cpu().numpy().astype(int),
@@ -67,6 +68,7 @@ def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True):
     torch.cuda.synchronize()
     res["out"] = outs.float().cpu().numpy().astype(np.float64)
     res["dev_err"] = int(s.dev_err.item())
+    res["guards_broken"] = s.check_guards() if guard else 0
     res["desc1"] = s.descriptors()
     res["pos1"] = s.pos_pool.cpu().numpy()
     res["session"] = s
@@ -119,6 +121,7 @@ def compare(cfg, gpu, heads_idx, T=None, report=None):
     T = float(np.float32(cfg.T if T is None else T))
     n = cfg.n
     rep = dict(checked=0, policy_exempt=0, topk_exempt=0, decode_checked=0)
+    assert gpu.get("guards_broken", 0) == 0, "a kernel wrote outside its buffer"
     # invariants over every head
     G = gpu["policy"].shape[0]
     assert np.all((gpu["policy"] >= 0) & (gpu["policy"] <= 4))
