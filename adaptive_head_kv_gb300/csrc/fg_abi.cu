@@ -118,10 +118,10 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
   float* bandcol = (float*)(ws + lse_bytes);
   uint8_t* cls = (uint8_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)));
   int32_t* sched = (int32_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)) +
-                              align_up((size_t)pd.B * pd.n));
+                              align_up((size_t)pd.B * pd.n));  // zeroed by the class kernel
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
-                                         punct_ids, n_punct, cls, s);
+                                         punct_ids, n_punct, cls, sched, s);
   if (e == cudaSuccess) {
     if (fg::profile_tc_supported(pd))
       e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, sched, dev_err, s);

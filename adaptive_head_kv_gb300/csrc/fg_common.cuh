@@ -106,4 +106,30 @@ __device__ __forceinline__ I block_exclusive_scan(I x, I* scratch, I* total) {
   return r;
 }
 
+// Launches `kernel` as a programmatic dependent of the kernel before it in
+// the stream: its CTAs may be scheduled while that kernel finishes, so they
+// must execute griddep_wait() before touching memory the previous kernels
+// write (the wait returns once those kernels have completed and their
+// writes are visible).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                              size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
 }  // namespace fg

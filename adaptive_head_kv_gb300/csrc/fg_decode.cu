@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
   // Programmatic dependent launch: this grid may be scheduled while the
   // previous kernel of the stream finishes; wait for it before any access,
   // then let the next kernel be scheduled early in turn.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  griddep_wait();
+  griddep_launch_dependents();
   const int wi = blockIdx.x;
   const int2 it = a.work[wi];
   const int g = it.x;
@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G, int HL) {
   constexpr int PL = D / 32;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x * 8 + warp;
   if (g >= G) return;
@@ -260,27 +260,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G,
 
 // Both kernels are launched as programmatic dependents of the kernel before
 // them in the stream, hiding the launch gaps between decode steps.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t s,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 template <typename T, int D>
 cudaError_t run(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(split_kernel<T, D>, a.n_work, kDecThreads, s, a, pd.HL, pd.sl2);
+  cudaError_t e = launch_pdl(split_kernel<T, D>, a.n_work, kDecThreads, 0, s, a, pd.HL, pd.sl2);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, s, a, pd.G, pd.HL);
+    e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, 0, s, a, pd.G, pd.HL);
   return e;
 }
 

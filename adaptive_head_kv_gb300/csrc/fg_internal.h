@@ -17,9 +17,11 @@ struct ProfileDims {
   float T, sl2;  // sl2 = scale * log2(e): scores are kept in base-2 units
 };
 
-// Token class per prompt position: bit 0 special, bit 1 punctuation.
+// Token class per prompt position: bit 0 special, bit 1 punctuation.  Also
+// zeroes the two work counters of the profiler passes (when non-null).
 cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
-                               const int32_t* punct, int np, uint8_t* cls, cudaStream_t s);
+                               const int32_t* punct, int np, uint8_t* cls, int32_t* counters,
+                               cudaStream_t s);
 
 // Row stride of the lse2 workspace: n rounded up to whole 128-row tiles.
 inline int lse_ld(int n) { return (n + 127) / 128 * 128; }

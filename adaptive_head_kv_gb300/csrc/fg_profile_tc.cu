@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
+  // the set-up above overlaps the previous kernel; its outputs are read below
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- producer (TMA)
@@ -508,13 +511,13 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = (unsigned)(units < 2LL * sms ? units : 2LL * sms);
-  e = cudaMemsetAsync(sched, 0, 2 * sizeof(int32_t), s);
-  if (e != cudaSuccess) return e;
-  profile_tc_kernel<1, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
-                                                      ld, nt, pd.w, pd.sl2, sched, err);
-  profile_tc_kernel<2, D><<<grid, kThreads, smem, s>>>(tq, tk, nlse2, colsum, bandcol, pd.G, pd.n,
-                                                      ld, nt, pd.w, pd.sl2, sched + 1, err);
-  return cudaGetLastError();
+  // the work counters were zeroed by the token-class kernel launched before
+  e = launch_pdl(profile_tc_kernel<1, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum, bandcol,
+                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, sched, err);
+  if (e == cudaSuccess)
+    e = launch_pdl(profile_tc_kernel<2, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum,
+                   bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, sched + 1, err);
+  return e;
 }
 
 }  // namespace

@@ -19,12 +19,16 @@ namespace fg {
 namespace {
 
 constexpr int kSelThreads = 256;
+constexpr int kSmemN = 8192;  // longest prompt whose column sums are staged in shared memory
 
 __global__ void token_class_kernel(const int32_t* __restrict__ ids, int count,
                                    const int32_t* __restrict__ special, int ns,
                                    const int32_t* __restrict__ punct, int np,
-                                   uint8_t* __restrict__ cls) {
+                                   uint8_t* __restrict__ cls, int32_t* __restrict__ counters) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i == 0 && counters) counters[0] = counters[1] = 0;  // the profiler passes' work counters
   if (i >= count) return;
   const int id = ids[i];
   cls[i] = (uint8_t)((id_in(id, special, ns) ? 1 : 0) | (id_in(id, punct, np) ? 2 : 0));
@@ -50,6 +54,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const uint8_t* __restrict__ cls, int n, int HL, int k, int w, float T,
     int8_t* __restrict__ policy, float* __restrict__ mass, int32_t* __restrict__ cost,
     uint8_t* __restrict__ keep, int32_t* __restrict__ kept) {
+  extern __shared__ float cs_smem[];  // the head's colsum when it fits (n <= kSmemN)
   __shared__ unsigned hist[256];
   __shared__ int s_bin, s_krem, s_eq;
   __shared__ int scan_scratch[33];
@@ -57,9 +62,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   __shared__ int ired[32];
   __shared__ int s_policy;
 
+  griddep_wait();
+  griddep_launch_dependents();
   const int g = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* c = colsum + (size_t)g * n;
+  if (n <= kSmemN) {  // read the head's column sums once
+    for (int j = threadIdx.x; j < n; j += blockDim.x) cs_smem[j] = c[j];
+    __syncthreads();
+    c = cs_smem;
+  }
   const float* bc = bandcol + (size_t)g * n;
   const uint8_t* cl = cls + (size_t)(g / HL) * n;
   uint8_t* kp = keep + (size_t)g * n;
@@ -190,17 +202,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 }  // namespace
 
 cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
-                               const int32_t* punct, int np, uint8_t* cls, cudaStream_t s) {
-  token_class_kernel<<<cdiv(count, 256), 256, 0, s>>>(ids, count, special, ns, punct, np, cls);
-  return cudaGetLastError();
+                               const int32_t* punct, int np, uint8_t* cls, int32_t* counters,
+                               cudaStream_t s) {
+  return launch_pdl(token_class_kernel, cdiv(count, 256), 256, 0, s, ids, count, special, ns,
+                    punct, np, cls, counters);
 }
 
 cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,
                           const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
                           uint8_t* keep, int32_t* kept, cudaStream_t s) {
-  select_kernel<<<pd.G, kSelThreads, 0, s>>>(colsum, bandcol, cls, pd.n, pd.HL, pd.k, pd.w, pd.T,
-                                             policy, mass, cost, keep, kept);
-  return cudaGetLastError();
+  const size_t smem = pd.n <= kSmemN ? (size_t)pd.n * sizeof(float) : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(select_kernel, pd.G, kSelThreads, smem, s, colsum, bandcol, cls, pd.n, pd.HL,
+                    pd.k, pd.w, pd.T, policy, mass, cost, keep, kept);
 }
 
 }  // namespace fg
