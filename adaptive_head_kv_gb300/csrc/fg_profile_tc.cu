@@ -152,17 +152,19 @@ __device__ __forceinline__ void lse_tile(uint32_t (&r)[2][32], float sl2, int c0
   m = mnew;
 }
 
-// Pass 2, one thread's 64 columns (starting at tile column c0) of a key row:
+// Pass 2, one thread's NC x 32 columns (starting at tile column c0) of a key row:
 // adds sum A to cs and the part inside the band to bs.  nl = negated base-2
 // LSEs of the tile's 128 queries (-inf past the prompt end).  Tile columns
 // c < lo precede the key (masked); columns c < band lie in the window.
-__device__ __forceinline__ void col_tile(const uint32_t (&r)[2][32], const float* nl, float sl2,
+template <int NC>
+__device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const float* nl, float sl2,
                                          int c0, int lo, int band, float& cs, float& bs) {
+  constexpr int kCols = NC * 32;
   const uint64_t s2 = pack2(sl2, sl2);
-  if (lo <= c0 && (band <= c0 || band >= c0 + kHalfCols)) {  // no per-element test
+  if (lo <= c0 && (band <= c0 || band >= c0 + kCols)) {  // no per-element test
     uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         const float4 L = *reinterpret_cast<const float4*>(nl + c0 + c * 32 + e);
@@ -180,12 +182,12 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[2][32], const float
       t += a0 + a1;
     }
     cs += t;
-    if (band >= c0 + kHalfCols) bs += t;
+    if (band >= c0 + kCols) bs += t;
     return;
   }
   float ta[4] = {0.f, 0.f, 0.f, 0.f}, ba[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int c = 0; c < 2; ++c)
+  for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int col = c0 + c * 32 + e;
@@ -388,16 +390,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         tc_fence_after();
-        uint32_t r[2][32];
-        tmem_ld32(lane_base + buf * kBlk, r[0]);
-        tmem_ld32(lane_base + buf * kBlk + 32, r[1]);
-        tmem_wait_ld(r[0]);
-        reg_barrier(r[1]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.sempty[buf]);
-        ++sseq;
         if (PASS == 1) {
+          uint32_t r[2][32];
+          tmem_ld32(lane_base + buf * kBlk, r[0]);
+          tmem_ld32(lane_base + buf * kBlk + 32, r[1]);
+          tmem_wait_ld(r[0]);
+          reg_barrier(r[1]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.sempty[buf]);
+          ++sseq;
           // key columns j = other0 + c are valid for j <= self and j < n
           const int lim = min(self + 1, n) - other0;
           lse_tile(r, sl2, c0, lim < kBlk ? max(lim, 0) : -1, m, l);
@@ -408,8 +410,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           // query columns i = other0 + c count for i >= self and lie in the
-          // window for i < self + w
-          col_tile(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
+          // window for i < self + w; the row is read in two halves of 32
+          // columns to keep the register pressure low
+          uint32_t r[1][32];
+          tmem_ld32(lane_base + buf * kBlk, r[0]);
+          tmem_wait_ld(r[0]);
+          col_tile<1>(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
+          tmem_ld32(lane_base + buf * kBlk + 32, r[0]);
+          tmem_wait_ld(r[0]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.sempty[buf]);
+          ++sseq;
+          col_tile<1>(r, s.nlse[ls], sl2, c0 + 32, self - other0, self + w - other0, cs, bs);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s.lempty[ls]);
           ++lseq;
