@@ -191,23 +191,17 @@ def run_ours(args, cfg, rank, world):
 
     from adaptive_head_kv_gb300 import fastgen as fg
     from adaptive_head_kv_gb300.session import FastGenSession, make_params
-    from synth import CONFIGS, make_workload, punct_ids, special_ids
+    from synth import make_workload_split, punct_ids, special_ids
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     dev = torch.device("cuda")
     n, steps, G, d = cfg.n, cfg.steps, cfg.G, cfg.d
     fg.lib()
-    w = make_workload(cfg, seed=rank)
-    pin = lambda t: t.pin_memory()
-    hQ = pin(w["Q"][:, :n].contiguous())
-    hK = pin(w["K"][:, :n].contiguous())
-    hV = pin(w["V"][:, :n].contiguous())
-    hq = pin(w["Q"][:, n:].transpose(0, 1).contiguous())
-    hk = pin(w["K"][:, n:].transpose(0, 1).contiguous())
-    hv = pin(w["V"][:, n:].transpose(0, 1).contiguous())
+    w = make_workload_split(cfg, seed=rank, pin=True)
+    hQ, hK, hV, hq, hk, hv = (w[x] for x in ("Q", "K", "V", "q", "k", "v"))
     ids_np = w["ids"]
-    hids = pin(torch.from_numpy(ids_np[:, :n].copy()))
-    hdec_ids = pin(torch.from_numpy(np.ascontiguousarray(ids_np[:, n:].T)))
+    hids = torch.from_numpy(ids_np[:, :n].copy()).pin_memory()
+    hdec_ids = torch.from_numpy(np.ascontiguousarray(ids_np[:, n:].T)).pin_memory()
     del w
     Q, K, V = hQ.to(dev), hK.to(dev), hV.to(dev)
     q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
@@ -385,6 +379,7 @@ def main():
     ap.add_argument("--config", default="llama7b")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=float, default=None, help="override the recover ratio")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (smaller cases for profiler captures)")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
@@ -399,6 +394,8 @@ def main():
     cfg = CONFIGS[args.config]
     if args.layers:
         cfg = cfg.with_(L=args.layers, name=f"{cfg.name}_L{args.layers}")
+    if args.T is not None:
+        cfg = cfg.with_(T=args.T, name=f"{cfg.name}_T{args.T:g}")
     if args.record_traffic:
         record_traffic(args.record_traffic, cfg.name, args.traffic_command)
         return

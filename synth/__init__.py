@@ -12,6 +12,7 @@ from .generator import (  # noqa: F401
     make_head,
     make_ids,
     make_workload,
+    make_workload_split,
     punct_ids,
     special_ids,
 )

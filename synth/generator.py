@@ -227,6 +227,35 @@ def _round(x: np.ndarray, dtype: str):
     return t.to(torch.bfloat16) if dtype == "bf16" else t.to(torch.float32)
 
 
+def make_workload_split(cfg: Config, seed: int = 0, threads: int | None = None, pin=False):
+    """The whole workload laid out as it is consumed: prompt tensors
+    Q, K, V [G, n, d] and per-step decode tensors q, k, v [steps, G, d] in the
+    working dtype (pinned host memory if `pin`), plus ids [B, n + steps].
+    Each head is generated once, straight into its slices."""
+    import torch
+
+    ids = make_ids(cfg, seed)
+    types = head_types(cfg, seed)
+    n, steps, d, G = cfg.n, cfg.steps, cfg.d, cfg.G
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    out = {}
+    for k in "QKV":
+        out[k] = torch.empty((G, n, d), dtype=tdt, pin_memory=pin)
+        out[k.lower()] = torch.empty((steps, G, d), dtype=tdt, pin_memory=pin)
+
+    def one(g):
+        q, k, v = make_head(cfg, seed, g, ids, types)
+        for name, x in (("Q", q), ("K", k), ("V", v)):
+            r = _round(x, cfg.dtype)
+            out[name][g] = r[:n]
+            out[name.lower()][:, g] = r[n:]
+
+    nthr = threads or min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(nthr) as ex:
+        list(ex.map(one, range(G)))
+    return dict(out, ids=ids, types=types)
+
+
 def make_workload(cfg: Config, seed: int = 0, heads=None, threads: int | None = None):
     """Rounded CPU tensors for a whole workload (or a subset of head indices).
 

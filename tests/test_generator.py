@@ -42,3 +42,15 @@ def test_normals_moments():
     ids, types = make_ids(cfg), head_types(cfg)
     _, _, v = make_head(cfg, 0, 17, ids, types)
     assert abs(v.mean()) < 0.01 and abs(v.std() - 1) < 0.01
+
+
+def test_split_layout_matches_heads():
+    from synth import make_workload_split
+
+    cfg = CONFIGS["tiny"].with_(L=2, H=3, n=40, steps=7)
+    a = make_workload_split(cfg, seed=5, threads=3)
+    b = make_workload(cfg, seed=5, threads=3)
+    n = cfg.n
+    for x in "QKV":
+        assert np.array_equal(a[x].numpy(), b[x][:, :n].numpy())
+        assert np.array_equal(a[x.lower()].numpy(), b[x][:, n:].transpose(0, 1).numpy())
