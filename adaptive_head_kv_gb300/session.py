@@ -87,6 +87,20 @@ class FastGenSession:
                                pos, out, self.dws, self.dev_err, self.stream)
         return out
 
+    def capture_decode(self, q, k, v, new_ids, pos0):
+        """Captures len(q) consecutive decode calls (inputs q, k, v
+        [steps, G, d] and new_ids [steps, B] on the device, positions pos0,
+        pos0 + 1, ...) as one CUDA graph; returns (graph, outs [steps, G, d]).
+        Replaying it runs those steps on the session's current caches.  The
+        plan and pools must not be reallocated between replays."""
+        steps = q.shape[0]
+        outs = self._empty((steps, self.G, self.p.d), self.tdtype)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for st in range(steps):
+                self.decode(q[st], k[st], v[st], new_ids[st], pos0 + st, out=outs[st])
+        return graph, outs
+
     def _empty(self, shape, dtype):
         if not self.guard:
             return torch.empty(shape, dtype=dtype, device=self.device)

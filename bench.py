@@ -210,23 +210,22 @@ def run_ours(args, cfg, rank, world):
     s = FastGenSession(p, special_ids(rank), punct_ids(rank), steps, device=dev)
     stream = torch.cuda.current_stream()
 
+    graph = None
+
     def one_step(record):
-        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(steps)] if record else None
         e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
         e0.record(stream)
         s.profile(Q, K, ids)
         e1.record(stream)
         s.compact(K, V)
         e2.record(stream)
-        for st in range(steps):
-            if record:
-                dec_ev[st][0].record(stream)
-            s.decode(q[st], k[st], v[st], dec_ids[st], n + st)
-            if record:
-                dec_ev[st][1].record(stream)
+        if graph is not None:  # the whole decode loop as one graph launch
+            graph.replay()
+        else:
+            for st in range(steps):
+                s.decode(q[st], k[st], v[st], dec_ids[st], n + st)
         e3.record(stream)
-        return e0, e1, e2, e3, dec_ev
+        return e0, e1, e2, e3
 
     def barrier():
         if world > 1:
@@ -235,9 +234,15 @@ def run_ours(args, cfg, rank, world):
 
     for _ in range(args.warmup):
         one_step(False)
+    if not args.no_graph:
+        # capture the decode loop once (same plan and pools every step), then
+        # warm the graph up like the rest
+        torch.cuda.synchronize()
+        graph, _ = s.capture_decode(q, k, v, dec_ids, n)
+        for _ in range(2):
+            one_step(False)
     barrier()
     per = []
-    dec_ms = np.zeros(steps)
     with Clocks(torch.cuda.current_device()) as clk:
         barrier()
         t_start = torch.cuda.Event(enable_timing=True)
@@ -247,15 +252,12 @@ def run_ours(args, cfg, rank, world):
             per.append(one_step(True))
         t_end.record(stream)
         barrier()
-    for ev in per:
-        for st in range(steps):
-            dec_ms[st] += ev[4][st][0].elapsed_time(ev[4][st][1])
     total_ms = t_start.elapsed_time(t_end)
-    prof_ms = np.mean([a.elapsed_time(b) for a, b, c, e, _ in per])
-    comp_ms = np.mean([b.elapsed_time(c) for a, b, c, e, _ in per])
-    decode_ms = np.mean([c.elapsed_time(e) for a, b, c, e, _ in per])
-    step_ms = np.mean([a.elapsed_time(e) for a, b, c, e, _ in per])
-    dec_ms /= args.steps
+    prof_ms = np.mean([a.elapsed_time(b) for a, b, c, e in per])
+    comp_ms = np.mean([b.elapsed_time(c) for a, b, c, e in per])
+    decode_ms = np.mean([c.elapsed_time(e) for a, b, c, e in per])
+    step_ms = np.mean([a.elapsed_time(e) for a, b, c, e in per])
+    dec_ms = np.full(steps, decode_ms / steps)  # per decode call, averaged over the loop
     assert fg.fastgen_read_error(s.dev_err) == fg.FG_OK
 
     # algorithmic work
@@ -380,6 +382,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=float, default=None, help="override the recover ratio")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every decode call from the host instead of one CUDA graph")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (smaller cases for profiler captures)")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
@@ -441,7 +445,8 @@ def main():
                                f"decode_steps={cfg.steps} T={cfg.T} r_l={cfg.r_l} r_f={cfg.r_f}",
                    "G": cfg.G, "parallelism": f"replicas x{world}",
                    "l2": "inputs and caches larger than L2 (no flush)",
-                   "step": "profile + plan + compact + all decode steps"},
+                   "step": "profile + plan + compact + all decode steps",
+                   "decode_launch": "host loop" if args.no_graph else "one CUDA graph per step"},
         "decode_tok_s": decode_tok_s, "decode_hbm_gbs": r["dec_gbs"],
         "phases_ms": {"profile": r["prof_ms"], "compact_plan": r["comp_ms"],
                       "decode_all_steps": r["decode_ms"], "decode_per_step": dec_launch_ms},

@@ -139,3 +139,29 @@ def test_guard_regions_catch_nothing_on_the_bench_shape():
     cfg = CONFIGS["llama7b"].with_(L=2, steps=16)
     gpu = run_gpu(cfg)
     assert gpu["guards_broken"] == 0 and gpu["dev_err"] == 0
+
+
+def test_decode_graph_replay_matches_host_loop():
+    """The decode loop captured as one CUDA graph gives the host loop's
+    outputs bit for bit, and can be replayed after a fresh prefill."""
+    from adaptive_head_kv_gb300.session import FastGenSession, make_params
+    from synth import make_workload_split, punct_ids, special_ids
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=4, n=300, steps=12)
+    gpu = run_gpu(cfg)
+    w = make_workload_split(cfg)
+    dev = torch.device("cuda")
+    n = cfg.n
+    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    s = FastGenSession(p, special_ids(), punct_ids(), cfg.steps)
+    Q, K, V = (w[x].to(dev) for x in "QKV")
+    q, k, v = (w[x].to(dev) for x in "qkv")
+    ids = torch.from_numpy(w["ids"]).to(dev)
+    dec_ids = ids[:, n:].transpose(0, 1).contiguous()
+    s.prefill(Q, K, V, ids[:, :n].contiguous())
+    graph, outs = s.capture_decode(q, k, v, dec_ids, n)
+    for _ in range(2):  # a fresh prefill resets the caches; the graph replays on them
+        s.prefill(Q, K, V, ids[:, :n].contiguous())
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(outs.float().cpu().numpy(), gpu["out"])
