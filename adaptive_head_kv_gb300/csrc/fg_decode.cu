@@ -230,23 +230,36 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G,
   const int g = blockIdx.x * 8 + warp;
   if (g >= G) return;
   const fg_head_desc hd = a.desc[g];
+  const size_t w0 = (size_t)hd.work_off;
+  // items in groups of 32: lane i holds item i's (max, sum); the weights are
+  // then broadcast while every lane sums its PL dimensions over the items
   float M = FG_NEG_INF;
-  for (int i = lane; i < hd.n_work; i += 32) M = fmaxf(M, a.part_ml[2 * (size_t)(hd.work_off + i)]);
+  for (int i = lane; i < hd.n_work; i += 32) M = fmaxf(M, a.part_ml[2 * (w0 + i)]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f, acc[PL];
 #pragma unroll
   for (int e = 0; e < PL; ++e) acc[e] = 0.f;
   if (M != FG_NEG_INF) {
-    for (int i = 0; i < hd.n_work; ++i) {
-      const size_t wi = (size_t)hd.work_off + i;
-      const float mi = a.part_ml[2 * wi];
-      if (mi == FG_NEG_INF) continue;
-      const float f = exp2f(mi - M);
-      L += f * a.part_ml[2 * wi + 1];
+    for (int base = 0; base < hd.n_work; base += 32) {
+      const int i = base + lane;
+      float wgt = 0.f;
+      if (i < hd.n_work) {
+        const float mi = a.part_ml[2 * (w0 + i)];
+        wgt = mi == FG_NEG_INF ? 0.f : exp2f(mi - M);
+        L += wgt * a.part_ml[2 * (w0 + i) + 1];
+      }
+      const int cnt = min(32, hd.n_work - base);
+#pragma unroll 4
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wgt, j);
+        const float* pa = a.part_acc + (w0 + base + j) * D + lane * PL;
 #pragma unroll
-      for (int e = 0; e < PL; ++e) acc[e] += f * a.part_acc[wi * D + lane * PL + e];
+        for (int e = 0; e < PL; ++e) acc[e] = fmaf(wj, pa[e], acc[e]);
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   }
   T* out = (T*)a.out + (size_t)g * D;
   const float inv = L > 0.f ? 1.f / L : 0.f;
