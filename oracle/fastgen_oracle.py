@@ -260,3 +260,55 @@ def decode_head(policy, keep, n, w, ids, Qall, Kall, Vall, special_ids, punct_id
         pos = decode_positions(policy, static, w, t)
         out[step] = attend(Qall[t], Kall[pos], Vall[pos], s)
     return out, pos
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention (the kdj.com article lists combining FastGen with
+# grouped-query attention as future work; the pages fix no rule for it).
+# Reading R10: query heads are profiled one by one exactly as above, each
+# against its group's shared K; the group keeps one cache, the union of its
+# members' final caches (a position is never-evicted if any member keeps it
+# so, else in the window if any member's window holds it); a generated token
+# is placed by the rule of the group's largest policy (the shortlist entries
+# are nested, so that rule keeps every token any member would keep); every
+# member attends over the shared cache.
+# ---------------------------------------------------------------------------
+
+def union_keep(keeps):
+    """Union of the members' keep codes (never-evicted beats window)."""
+    keeps = np.asarray(keeps)
+    static = (keeps == KEEP_STATIC).any(axis=0)
+    window = (keeps == KEEP_WINDOW).any(axis=0)
+    return np.where(static, KEEP_STATIC, np.where(window, KEEP_WINDOW, DROP)).astype(np.uint8)
+
+
+def profile_group(Qs, K, ids, special_ids, punct_ids, T, r_l, r_f, scale=None):
+    """Profiles every query head of a group against the shared K.  Returns
+    (member results, group keep codes, group policy)."""
+    members = [profile_head(Q, K, ids, special_ids, punct_ids, T, r_l, r_f, scale) for Q in Qs]
+    keep = union_keep([m["keep"] for m in members])
+    return members, keep, max(m["policy"] for m in members)
+
+
+def decode_group(policy, keep, n, w, ids, Qalls, Kall, Vall, special_ids, punct_ids, steps,
+                 scale=None):
+    """Generation over a group's shared cache: the token at each position is
+    placed by the group policy's rule and every member attends with its own
+    query.  Returns (out [members, steps, d], final cache positions)."""
+    Kall = np.asarray(Kall, dtype=np.float64)
+    Vall = np.asarray(Vall, dtype=np.float64)
+    d = Kall.shape[1]
+    s = default_scale(d) if scale is None else scale
+    sset, pset = set(int(x) for x in special_ids), set(int(x) for x in punct_ids)
+    static = [int(j) for j in np.nonzero(np.asarray(keep) == KEEP_STATIC)[0]]
+    out = np.zeros((len(Qalls), steps, d))
+    pos = np.array(static, dtype=np.int64)
+    for step in range(steps):
+        t = n + step
+        tau = int(ids[t])
+        if stores_static(policy, tau in sset, tau in pset):
+            static.append(t)
+        pos = decode_positions(policy, static, w, t)
+        for m, Qall in enumerate(Qalls):
+            out[m, step] = attend(np.asarray(Qall, dtype=np.float64)[t], Kall[pos], Vall[pos], s)
+    return out, pos

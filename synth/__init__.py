@@ -9,7 +9,10 @@ from .generator import (  # noqa: F401
     CONFIGS,
     HEAD_TYPES,
     head_types,
+    kv_of,
     make_head,
+    make_kv,
+    make_q,
     make_ids,
     make_workload,
     make_workload_split,

@@ -110,11 +110,20 @@ class Config:
     r_f: float
     mix: tuple = (0.15, 0.20, 0.35, 0.30)  # special / punct / local / broad
     one_of_each: bool = False  # tiny: head h of each layer has type h % 4
+    Hkv: int = 0  # key/value heads per layer (grouped-query attention); 0 = H
     extra: dict = field(default_factory=dict, compare=False)
 
     @property
     def G(self) -> int:
         return self.B * self.L * self.H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
+
+    @property
+    def Gkv(self) -> int:
+        return self.B * self.L * self.kv_heads
 
     def with_(self, **kw) -> "Config":
         return replace(self, **kw)
@@ -195,29 +204,61 @@ def _rope(c: np.ndarray, positions: np.ndarray, base: float = 10000.0) -> np.nda
     return out
 
 
-def make_head(cfg: Config, seed: int, g: int, ids: np.ndarray, types: np.ndarray):
-    """float64 (Q, K, V), each [n + steps, d], of head instance g = (b*L + l)*H + h."""
+def kv_of(cfg: Config, g: int) -> int:
+    """Key/value head of query head g: head h of a layer uses kv head h // (H / Hkv)."""
     b, rem = divmod(g, cfg.L * cfg.H)
     l, h = divmod(rem, cfg.H)
+    return (b * cfg.L + l) * cfg.kv_heads + h // (cfg.H // cfg.kv_heads)
+
+
+def _plant(cfg: Config, seed: int, l: int, kv: int, kind: int) -> np.ndarray:
+    # one planted vector per (layer, head) without groups; per type in a group
+    if cfg.kv_heads == cfg.H:
+        return _normal(_key(seed, _S_PLANT, l, kv), cfg.d)
+    return _normal(_key(seed, _S_PLANT, l, kv, 100 + kind), cfg.d)
+
+
+def make_q(cfg: Config, seed: int, g: int, ids: np.ndarray, types: np.ndarray) -> np.ndarray:
+    """float64 Q [n + steps, d] of query head g = (b*L + l)*H + h."""
+    b, rem = divmod(g, cfg.L * cfg.H)
+    l, h = divmod(rem, cfg.H)
+    kv = h // (cfg.H // cfg.kv_heads)
     total, d = cfg.n + cfg.steps, cfg.d
-    kind = HEAD_TYPES[types[l, h]]
+    kind = int(types[l, h])
     Q = _normal(_key(seed, _S_Q, b, l, h), total * d).reshape(total, d)
-    K = _normal(_key(seed, _S_K, b, l, h), total * d).reshape(total, d)
-    V = _normal(_key(seed, _S_V, b, l, h), total * d).reshape(total, d)
-    plant = _normal(_key(seed, _S_PLANT, l, h), d)
-    if kind == "special":
-        mask = np.isin(ids[b], special_ids(seed))
-        K[mask] += 4.0 * plant
+    plant = _plant(cfg, seed, l, kv, kind)
+    if HEAD_TYPES[kind] in ("special", "punct"):
         Q += 4.0 * plant
-    elif kind == "punct":
-        mask = np.isin(ids[b], punct_ids(seed))
-        K[mask] += 4.0 * plant
-        Q += 4.0 * plant
-    elif kind == "local":
-        r = _rope(3.0 * plant, np.arange(total))
-        Q += r
-        K += r
-    return Q, K, V
+    elif HEAD_TYPES[kind] == "local":
+        Q += _rope(3.0 * plant, np.arange(total))
+    return Q
+
+
+def make_kv(cfg: Config, seed: int, c: int, ids: np.ndarray, types: np.ndarray):
+    """float64 (K, V) [n + steps, d] of key/value head c = (b*L + l)*Hkv + kv,
+    carrying the planted structure of every query head type in its group."""
+    b, rem = divmod(c, cfg.L * cfg.kv_heads)
+    l, kv = divmod(rem, cfg.kv_heads)
+    total, d = cfg.n + cfg.steps, cfg.d
+    r = cfg.H // cfg.kv_heads
+    K = _normal(_key(seed, _S_K, b, l, kv), total * d).reshape(total, d)
+    V = _normal(_key(seed, _S_V, b, l, kv), total * d).reshape(total, d)
+    for kind in sorted(set(int(t) for t in types[l, kv * r:(kv + 1) * r])):
+        plant = _plant(cfg, seed, l, kv, kind)
+        if HEAD_TYPES[kind] == "special":
+            K[np.isin(ids[b], special_ids(seed))] += 4.0 * plant
+        elif HEAD_TYPES[kind] == "punct":
+            K[np.isin(ids[b], punct_ids(seed))] += 4.0 * plant
+        elif HEAD_TYPES[kind] == "local":
+            K += _rope(3.0 * plant, np.arange(total))
+    return K, V
+
+
+def make_head(cfg: Config, seed: int, g: int, ids: np.ndarray, types: np.ndarray):
+    """float64 (Q, K, V), each [n + steps, d], of query head g and its
+    key/value head."""
+    K, V = make_kv(cfg, seed, kv_of(cfg, g), ids, types)
+    return make_q(cfg, seed, g, ids, types), K, V
 
 
 def _round(x: np.ndarray, dtype: str):
@@ -228,39 +269,50 @@ def _round(x: np.ndarray, dtype: str):
 
 
 def make_workload_split(cfg: Config, seed: int = 0, threads: int | None = None, pin=False):
-    """The whole workload laid out as it is consumed: prompt tensors
-    Q, K, V [G, n, d] and per-step decode tensors q, k, v [steps, G, d] in the
-    working dtype (pinned host memory if `pin`), plus ids [B, n + steps].
-    Each head is generated once, straight into its slices."""
+    """The whole workload laid out as it is consumed: prompt tensors Q
+    [G, n, d] and K, V [Gkv, n, d], and per-step decode tensors q [steps, G, d]
+    and k, v [steps, Gkv, d], in the working dtype (pinned host memory if
+    `pin`), plus ids [B, n + steps].  Each head is generated once, straight
+    into its slices."""
     import torch
 
     ids = make_ids(cfg, seed)
     types = head_types(cfg, seed)
-    n, steps, d, G = cfg.n, cfg.steps, cfg.d, cfg.G
+    n, steps, d = cfg.n, cfg.steps, cfg.d
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     out = {}
-    for k in "QKV":
-        out[k] = torch.empty((G, n, d), dtype=tdt, pin_memory=pin)
-        out[k.lower()] = torch.empty((steps, G, d), dtype=tdt, pin_memory=pin)
+    for k, rows in (("Q", cfg.G), ("K", cfg.Gkv), ("V", cfg.Gkv)):
+        out[k] = torch.empty((rows, n, d), dtype=tdt, pin_memory=pin)
+        out[k.lower()] = torch.empty((steps, rows, d), dtype=tdt, pin_memory=pin)
 
-    def one(g):
-        q, k, v = make_head(cfg, seed, g, ids, types)
-        for name, x in (("Q", q), ("K", k), ("V", v)):
-            r = _round(x, cfg.dtype)
-            out[name][g] = r[:n]
-            out[name.lower()][:, g] = r[n:]
+    def put(name, i, x):
+        r = _round(x, cfg.dtype)
+        out[name][i] = r[:n]
+        out[name.lower()][:, i] = r[n:]
+
+    def one(i):
+        if i < cfg.G:
+            put("Q", i, make_q(cfg, seed, i, ids, types))
+        else:
+            c = i - cfg.G
+            k, v = make_kv(cfg, seed, c, ids, types)
+            put("K", c, k)
+            put("V", c, v)
 
     nthr = threads or min(32, os.cpu_count() or 1)
     with ThreadPoolExecutor(nthr) as ex:
-        list(ex.map(one, range(G)))
+        list(ex.map(one, range(cfg.G + cfg.Gkv)))
     return dict(out, ids=ids, types=types)
 
 
 def make_workload(cfg: Config, seed: int = 0, heads=None, threads: int | None = None):
-    """Rounded CPU tensors for a whole workload (or a subset of head indices).
+    """Rounded CPU tensors for a whole workload (or a subset of query-head
+    indices).
 
-    Returns dict(Q, K, V: [len(heads), n + steps, d] in the working dtype,
-    ids: [B, n + steps] int32, types: [L, H], heads: the head indices).
+    Returns dict(Q: [len(heads), n + steps, d]; K, V: the same rows for
+    their key/value heads (one per query head listed; without groups this is
+    each head's own K/V); Kg, Vg: [Gkv, n + steps, d] when heads is None;
+    ids: [B, n + steps] int32, types: [L, H], heads: the query-head indices).
     """
     import torch
 
