@@ -28,6 +28,9 @@ fg_status check_params(const fg_params* p) {
   if (!(p->T > 0.f && p->T <= 1.f)) return FG_EINVAL;
   if (!(p->r_l >= 0.f && p->r_l <= 1.f) || !(p->r_f >= 0.f && p->r_f <= 1.f)) return FG_EINVAL;
   if (!(p->scale >= 0.f) || isinf(p->scale)) return FG_EINVAL;
+  if (p->Hkv < 0 || (p->Hkv > 0 && p->H % p->Hkv != 0)) return FG_EINVAL;
+  const int R = p->Hkv > 0 ? p->H / p->Hkv : 1;
+  if (R != 1 && R != 2 && R != 4 && R != 8) return FG_EDTYPE;
   return FG_OK;
 }
 
@@ -36,6 +39,11 @@ fg::ProfileDims dims(const fg_params* p) {
   pd.B = p->B;
   pd.HL = p->L * p->H;
   pd.G = p->B * pd.HL;
+  pd.H = p->H;
+  pd.Hkv = p->Hkv > 0 ? p->Hkv : p->H;
+  pd.R = p->H / pd.Hkv;
+  pd.HLkv = p->L * pd.Hkv;
+  pd.Gkv = p->B * pd.HLkv;
   pd.n = p->n;
   pd.d = p->d;
   pd.dtype = p->dtype;
@@ -57,12 +65,16 @@ fg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FG_OK : FG_ECUD
 
 size_t elem_bytes(const fg_params* p) { return p->dtype == FG_BF16 ? 2 : 4; }
 
-// plan buffer: [G descriptors][2 x int64 totals][work list]
-size_t plan_desc_bytes(int G) { return align_up((size_t)G * sizeof(fg_head_desc)); }
+// plan buffer: [Gkv descriptors][Gkv x int2 group info][2 x int64 totals][work list]
+size_t plan_desc_bytes(int Gkv) { return align_up((size_t)Gkv * sizeof(fg_head_desc)); }
+size_t plan_cinfo_bytes(int Gkv) { return align_up((size_t)Gkv * sizeof(int2)); }
+size_t plan_work_offset(int Gkv) { return plan_desc_bytes(Gkv) + plan_cinfo_bytes(Gkv) + kAlign; }
+int kv_count(const fg_params* p) { return p->B * p->L * (p->Hkv > 0 ? p->Hkv : p->H); }
+int group_size(const fg_params* p) { return p->Hkv > 0 ? p->H / p->Hkv : 1; }
 size_t plan_max_work(const fg_params* p, int32_t max_new) {
-  const size_t G = (size_t)p->B * p->L * p->H;
+  const size_t Gkv = (size_t)kv_count(p);
   const int w = ratio_count(p->r_l, p->n);
-  return G * (size_t)(cdiv(p->n + max_new, fg::kRowsPerWork) + cdiv(w, fg::kRowsPerWork));
+  return Gkv * (size_t)(cdiv(p->n + max_new, fg::kRowsPerWork) + cdiv(w, fg::kRowsPerWork));
 }
 
 }  // namespace
@@ -135,26 +147,28 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
 
 size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens) {
   if (check_params(p) != FG_OK || max_new_tokens < 0) return 0;
-  const int G = p->B * p->L * p->H;
-  return plan_desc_bytes(G) + kAlign + plan_max_work(p, max_new_tokens) * sizeof(int2);
+  return plan_work_offset(kv_count(p)) + plan_max_work(p, max_new_tokens) * sizeof(int2);
 }
 
-fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const int32_t* cost,
+fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const uint8_t* keep,
                                int32_t max_new_tokens, void* plan, size_t plan_bytes,
                                fg_plan_info* info, void* stream) {
   fg_status st = check_params(p);
   if (st != FG_OK) return st;
-  if (!policy || !cost || !plan || !info || max_new_tokens < 0) return FG_EINVAL;
-  if (!aligned(plan, kAlign) || !aligned(cost, 4)) return FG_EINVAL;
+  if (!policy || !keep || !plan || !info || max_new_tokens < 0) return FG_EINVAL;
+  if (!aligned(plan, kAlign)) return FG_EINVAL;
   if ((long long)p->n + max_new_tokens > 0x7fffffffLL - fg::kRowsPerWork) return FG_EINVAL;
   if (plan_bytes < fastgen_plan_bytes(p, max_new_tokens)) return FG_EWORKSPACE;
   const fg::ProfileDims pd = dims(p);
   char* base = (char*)plan;
   fg_head_desc* desc = (fg_head_desc*)base;
-  long long* totals = (long long*)(base + plan_desc_bytes(pd.G));
-  int2* work = (int2*)(base + plan_desc_bytes(pd.G) + kAlign);
+  int2* cinfo = (int2*)(base + plan_desc_bytes(pd.Gkv));
+  long long* totals = (long long*)(base + plan_desc_bytes(pd.Gkv) + plan_cinfo_bytes(pd.Gkv));
+  int2* work = (int2*)(base + plan_work_offset(pd.Gkv));
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = fg::launch_plan(pd.G, pd.w, max_new_tokens, policy, cost, desc, work, totals, s);
+  cudaError_t e = fg::launch_group(pd, policy, keep, cinfo, s);
+  if (e == cudaSuccess)
+    e = fg::launch_plan(pd.Gkv, pd.w, max_new_tokens, cinfo, desc, work, totals, s);
   long long h[2] = {0, 0};
   if (e == cudaSuccess) e = cudaMemcpyAsync(h, totals, sizeof(h), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -184,7 +198,7 @@ fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, cons
 
 size_t fastgen_decode_workspace_bytes(const fg_params* p, const fg_plan_info* info) {
   if (check_params(p) != FG_OK || !info || info->n_work < 0) return 0;
-  const size_t nw = (size_t)info->n_work;
+  const size_t nw = (size_t)info->n_work * group_size(p);  // one partial per item and query
   return align_up(nw * 2 * sizeof(float)) + align_up(nw * p->d * sizeof(float));
 }
 
@@ -212,7 +226,7 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
   char* base = (char*)plan;
   fg::DecodeArgs a;
   a.desc = (fg_head_desc*)base;
-  a.work = (const int2*)(base + plan_desc_bytes(pd.G) + kAlign);
+  a.work = (const int2*)(base + plan_work_offset(pd.Gkv));
   a.n_work = info->n_work;
   a.Kp = K_pool;
   a.Vp = V_pool;
@@ -229,7 +243,7 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
   a.out = out;
   char* ws = (char*)workspace;
   a.part_ml = (float*)ws;
-  a.part_acc = (float*)(ws + align_up((size_t)info->n_work * 2 * sizeof(float)));
+  a.part_acc = (float*)(ws + align_up((size_t)info->n_work * pd.R * 2 * sizeof(float)));
   a.dev_err = dev_err;
   if (info->n_work == 0) {
     cudaError_t e = cudaMemsetAsync(out, 0, (size_t)pd.G * pd.d * elem_bytes(p),

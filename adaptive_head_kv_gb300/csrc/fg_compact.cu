@@ -7,7 +7,8 @@
 //                                  for max_new_tokens appended rows;
 //   [win_off, win_off + w)         SPFL heads only: the window ring, the row
 //                                  of position t at slot t mod w.
-// The plan kernel lays heads out by an exclusive scan of their row counts
+// One cache per key/value head holds the union of its query heads' caches.
+// The plan kernel lays caches out by an exclusive scan of their row counts
 // and also emits the decode work list (one item per kRowsPerWork rows).
 #include "fg_common.cuh"
 #include "fg_internal.h"
@@ -18,9 +19,46 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kCompactThreads = 256;
 
+// Union of a key/value head's members (query heads g0 .. g0 + R - 1): the
+// group policy is the largest member policy (the placement rules are nested
+// along the shortlist) and the never-evicted prompt set is the union of the
+// members' (a position any member keeps so).
+__device__ __forceinline__ int union_code(const uint8_t* __restrict__ keep, size_t g0, int R, int n,
+                                          int j) {
+  int any_static = 0, any_window = 0;
+  for (int m = 0; m < R; ++m) {
+    const int c = keep[(g0 + m) * (size_t)n + j];
+    any_static |= c == FG_KEEP_STATIC;
+    any_window |= c == FG_KEEP_WINDOW;
+  }
+  return any_static ? FG_KEEP_STATIC : (any_window ? FG_KEEP_WINDOW : FG_KEEP_DROP);
+}
+
+__global__ void __launch_bounds__(256) group_kernel(const int8_t* __restrict__ policy,
+                                                    const uint8_t* __restrict__ keep, int n,
+                                                    int H, int R, int2* __restrict__ cinfo) {
+  __shared__ int red[8];
+  const int c = blockIdx.x;
+  const int Hkv = H / R;
+  const size_t g0 = (size_t)(c / Hkv) * H + (size_t)(c % Hkv) * R;
+  int cnt = 0;
+  for (int j = threadIdx.x; j < n; j += blockDim.x)
+    cnt += union_code(keep, g0, R, n, j) == FG_KEEP_STATIC;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0, pol = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+    for (int m = 0; m < R; ++m) pol = max(pol, (int)policy[g0 + m]);
+    cinfo[c] = make_int2(pol, tot);
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
-    const int8_t* __restrict__ policy, const int32_t* __restrict__ cost, int G, int w,
-    int reserve, fg_head_desc* __restrict__ desc, long long* __restrict__ totals) {
+    const int2* __restrict__ cinfo, int G, int w, int reserve, fg_head_desc* __restrict__ desc,
+    long long* __restrict__ totals) {
   __shared__ long long scr64[33];
   __shared__ int scr32[33];
   long long row_base = 0;
@@ -30,12 +68,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     long long rows = 0;
     int works = 0, p = 0, n_static = 0, cap = 0, wg = 0;
     if (g < G) {
-      p = policy[g];
-      n_static = (p == FG_POLICY_SPFL) ? cost[(size_t)g * 5 + 2] : cost[(size_t)g * 5 + p];
+      const int2 ci = cinfo[g];
+      p = ci.x;
+      n_static = ci.y;
       cap = n_static + reserve;
       wg = (p == FG_POLICY_SPFL) ? w : 0;
       rows = (long long)cap + wg;
-      works = cdiv(cap, kRowsPerWork) + cdiv(wg, kRowsPerWork);
+      works = max(1, cdiv(cap, kRowsPerWork) + cdiv(wg, kRowsPerWork));
     }
     long long rtot;
     int wtot;
@@ -75,16 +114,17 @@ __global__ void worklist_kernel(const fg_head_desc* __restrict__ desc, int G,
 template <typename T, int D>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
     const T* __restrict__ K, const T* __restrict__ V, const uint8_t* __restrict__ keep,
-    const fg_head_desc* __restrict__ desc, int n, T* __restrict__ Kp, T* __restrict__ Vp,
-    int32_t* __restrict__ posp) {
+    const fg_head_desc* __restrict__ desc, int n, int H, int R, T* __restrict__ Kp,
+    T* __restrict__ Vp, int32_t* __restrict__ posp) {
   constexpr int E = Vec16<T>::kElems;
   constexpr int LPR = D / E;  // 16-byte vectors per row
   __shared__ int scr[33];
   __shared__ int src_pos[kCompactThreads];
   __shared__ long long dst_row[kCompactThreads];
-  const int g = blockIdx.x;
+  const int g = blockIdx.x;  // key/value head
   const fg_head_desc hd = desc[g];
-  const uint8_t* kg = keep + (size_t)g * n;
+  const int Hkv = H / R;
+  const size_t g0 = (size_t)(g / Hkv) * H + (size_t)(g % Hkv) * R;  // its first query head
   // empty markers: reserve rows of the static segment and every ring slot
   for (int r = hd.n_static + threadIdx.x; r < hd.static_cap; r += blockDim.x)
     posp[hd.off + r] = -1;
@@ -93,7 +133,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
   int static_seen = 0;
   for (int base = 0; base < n; base += blockDim.x) {
     const int j = base + threadIdx.x;
-    const int code = j < n ? kg[j] : FG_KEEP_DROP;
+    const int code = j < n ? union_code(keep, g0, R, n, j) : FG_KEEP_DROP;
     const int is_static = code == FG_KEEP_STATIC;
     const int is_kept = code != FG_KEEP_DROP;
     int st_total, kept_total;
@@ -128,17 +168,23 @@ template <typename T, int D>
 cudaError_t run_compact(const ProfileDims& pd, const void* K, const void* V, const uint8_t* keep,
                         const fg_head_desc* desc, void* Kp, void* Vp, int32_t* posp,
                         cudaStream_t s) {
-  compact_kernel<T, D><<<pd.G, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
-                                                        pd.n, (T*)Kp, (T*)Vp, posp);
+  compact_kernel<T, D><<<pd.Gkv, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
+                                                          pd.n, pd.H, pd.R, (T*)Kp, (T*)Vp, posp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_plan(int G, int w, int reserve, const int8_t* policy, const int32_t* cost,
-                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(policy, cost, G, w, reserve, desc, totals);
-  worklist_kernel<<<cdiv(G, 256), 256, 0, s>>>(desc, G, work);
+cudaError_t launch_group(const ProfileDims& pd, const int8_t* policy, const uint8_t* keep,
+                         int2* cinfo, cudaStream_t s) {
+  group_kernel<<<pd.Gkv, 256, 0, s>>>(policy, keep, pd.n, pd.H, pd.R, cinfo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(int Gkv, int w, int reserve, const int2* cinfo, fg_head_desc* desc,
+                        int2* work, long long* totals, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(cinfo, Gkv, w, reserve, desc, totals);
+  worklist_kernel<<<cdiv(Gkv, 256), 256, 0, s>>>(desc, Gkv, work);
   return cudaGetLastError();
 }
 

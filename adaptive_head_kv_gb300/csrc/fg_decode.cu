@@ -2,17 +2,23 @@
 // What to Discard, Method: head-specific KV caches, keys/values appended at
 // each step, the prompt-time policy reused during generation).
 //
-// Split-K over a static work list: item (g, c) covers up to kRowsPerWork
-// rows of head g's never-evicted segment or of its window ring.  Each CTA
+// Split-K over a static work list: item (c, i) covers up to kRowsPerWork
+// rows of cache c's never-evicted segment or of its window ring (one cache
+// per key/value head; its R query heads all attend over it).  Each CTA
 //   * places the new token if its slot falls in the item (the only writer of
 //     that row; it attends with the new key/value from registers, so no CTA
 //     reads a row written in this launch),
-//   * streams its K/V rows with 16-byte loads (one row per LPR lanes), does
-//     the q.k dot in fp32 and an online base-2 softmax per lane group,
-//   * writes (max, sum, acc[d]) for the item.
-// A second launch merges the items of each head (log-sum-exp merge), writes
-// out[g] and bumps the head's never-evicted row count.  HBM-bound: no tensor
-// cores (a single query per head gives no reuse of the K/V rows).
+//   * streams its K/V rows once with 16-byte loads (one row per LPR lanes)
+//     and scores every row against the R queries of the group: fp32 dots
+//     (fp64 for fp32 inputs) and an online base-2 softmax per lane group and
+//     query,
+//   * writes (max, sum, acc[d]) per query for the item.
+// A second launch merges each query head's items (log-sum-exp merge), writes
+// out[g] and bumps the cache's never-evicted row count.  Both are launched as
+// programmatic dependents of the kernel before them.  HBM-bound: no tensor
+// cores (at most 8 queries share a K/V row).
+#include <type_traits>
+
 #include "fg_common.cuh"
 #include "fg_internal.h"
 
@@ -21,7 +27,6 @@ namespace {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kUnroll = 4;
 
 struct Placement {
   bool st;        // joins the never-evicted segment
@@ -29,9 +34,10 @@ struct Placement {
   bool ring_put;  // goes into the window ring
 };
 
-__device__ __forceinline__ Placement place(const fg_head_desc& hd, const DecodeArgs& a, int HL,
-                                           int g) {
-  const int tau = a.new_ids[g / HL];
+// c: cache (key/value head) index; HLkv = L * Hkv caches per sequence.
+__device__ __forceinline__ Placement place(const fg_head_desc& hd, const DecodeArgs& a, int HLkv,
+                                           int c) {
+  const int tau = a.new_ids[c / HLkv];
   const bool is_s = id_in(tau, a.special, a.ns), is_p = id_in(tau, a.punct, a.np);
   Placement pl;
   pl.st = joins_static(hd.policy, is_s, is_p);
@@ -41,26 +47,29 @@ __device__ __forceinline__ Placement place(const fg_head_desc& hd, const DecodeA
   return pl;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, int HL, float sl2) {
+// R = queries per cache (group size).  Rows are unrolled by U per warp so
+// that 2 * U 16-byte loads per thread are in flight.
+template <typename T, int D, int R>
+__global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, int H, int HLkv,
+                                                           float sl2) {
   constexpr int E = Vec16<T>::kElems;
   constexpr int LPR = D / E;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp per load
   constexpr int STEP = kDecWarps * RPW;
-  __shared__ float sm_m[kDecWarps], sm_l[kDecWarps];
-  __shared__ float sm_acc[kDecWarps][D];
+  constexpr int U = R == 1 ? 4 : (R == 2 ? 2 : 1);
+  constexpr bool kWide = sizeof(T) == 4;  // fp32 inputs: fp64 dot, scaled once
+  using Score = typename std::conditional<kWide, double, float>::type;
+  __shared__ float sm_m[R][kDecWarps], sm_l[R][kDecWarps];
+  __shared__ float sm_acc[R][kDecWarps][D];
 
-  // Programmatic dependent launch: this grid may be scheduled while the
-  // previous kernel of the stream finishes; wait for it before any access,
-  // then let the next kernel be scheduled early in turn.
   griddep_wait();
   griddep_launch_dependents();
   const int wi = blockIdx.x;
   const int2 it = a.work[wi];
-  const int g = it.x;
+  const int c = it.x;  // cache
   int chunk = it.y;
-  const fg_head_desc hd = a.desc[g];
-  const Placement pl = place(hd, a, HL, g);
+  const fg_head_desc hd = a.desc[c];
+  const Placement pl = place(hd, a, HLkv, c);
   const int nsc = cdiv(hd.static_cap, kRowsPerWork);
   const bool ring = chunk >= nsc;
   int r0, r1, new_slot, evict = -1;
@@ -82,8 +91,8 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
   }
   T* Kp = (T*)a.Kp;
   T* Vp = (T*)a.Vp;
-  const T* kn = (const T*)a.k_new + (size_t)g * D;
-  const T* vn = (const T*)a.v_new + (size_t)g * D;
+  const T* kn = (const T*)a.k_new + (size_t)c * D;
+  const T* vn = (const T*)a.v_new + (size_t)c * D;
   if (new_slot >= r0 && new_slot < r1) {
     for (int v = threadIdx.x; v < LPR; v += blockDim.x) {
       const size_t d = (size_t)(base + new_slot) * D + v * E;
@@ -96,25 +105,31 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, gl = lane % LPR;
-  // fp32 inputs: the dot is accumulated in fp64 and scaled once, so that
-  // rounding does not perturb the scores key by key (the fp32 path is held
-  // to 1e-5 on the outputs); bf16 inputs use an fp32 dot on a pre-scaled q.
-  constexpr bool kWide = sizeof(T) == 4;
-  float qf[E];
-  load16((const T*)a.q + (size_t)g * D + gl * E, qf);
-  if (!kWide) {
+  const int Hkv = H / R;
+  const size_t g0 = (size_t)(c / Hkv) * H + (size_t)(c % Hkv) * R;  // first query head
+  float qf[R][E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) qf[e] *= sl2;
+  for (int q = 0; q < R; ++q) {
+    load16((const T*)a.q + (g0 + q) * D + gl * E, qf[q]);
+    if (!kWide) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) qf[q][e] *= sl2;
+    }
   }
-  float m = FG_NEG_INF, l = 0.f, acc[E];
+  float m[R], l[R], acc[R][E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int q = 0; q < R; ++q) {
+    m[q] = FG_NEG_INF;
+    l[q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[q][e] = 0.f;
+  }
 
-  for (int rb = r0; rb < r1; rb += STEP * kUnroll) {
-    uint4 kv[kUnroll], vv[kUnroll];
-    bool ok[kUnroll];
+  for (int rb = r0; rb < r1; rb += STEP * U) {
+    uint4 kv[U], vv[U];
+    bool ok[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int r = rb + (u * kDecWarps + warp) * RPW + grp;
       const bool in = r < r1;
       const bool fresh = r == new_slot;
@@ -129,112 +144,132 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
         vv[u] = make_uint4(0, 0, 0, 0);
       }
     }
-    float s[kUnroll];
-    float mloc = FG_NEG_INF;
+    // fp32 inputs keep the score in fp64 and round the running max up to an
+    // integer, so that score - max and the merges of partial maxima are exact
+    // (an fp32 score of ~185 in base-2 units carries ~1e-5 of rounding)
+    Score sc[U][R];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       float f[E];
       unpack16(kv[u], f, (const T*)nullptr);
-      float dot;
-      if (kWide) {
-        double dd = 0.0;
 #pragma unroll
-        for (int e = 0; e < E; ++e) dd = fma((double)qf[e], (double)f[e], dd);
+      for (int q = 0; q < R; ++q) {
+        Score dot;
+        if (kWide) {
+          double dd = 0.0;
 #pragma unroll
-        for (int o = LPR / 2; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
-        dot = (float)(dd * (double)sl2);
-      } else {
-        dot = 0.f;
+          for (int e = 0; e < E; ++e) dd = fma((double)qf[q][e], (double)f[e], dd);
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qf[e], f[e], dot);
+          for (int o = LPR / 2; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+          dot = (Score)(dd * (double)sl2);
+        } else {
+          float df = 0.f;
 #pragma unroll
-        for (int o = LPR / 2; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          for (int e = 0; e < E; ++e) df = fmaf(qf[q][e], f[e], df);
+#pragma unroll
+          for (int o = LPR / 2; o >= 1; o >>= 1) df += __shfl_xor_sync(0xffffffffu, df, o);
+          dot = (Score)df;
+        }
+        sc[u][q] = ok[u] ? dot : (Score)FG_NEG_INF;
       }
-      s[u] = ok[u] ? dot : FG_NEG_INF;
-      mloc = fmaxf(mloc, s[u]);
     }
-    const float mnew = fmaxf(m, mloc);
-    if (mnew != FG_NEG_INF) {
-      const float corr = exp2f(m - mnew);
-      l *= corr;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] *= corr;
+    for (int q = 0; q < R; ++q) {
+      Score mloc = (Score)FG_NEG_INF;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < U; ++u) mloc = sc[u][q] > mloc ? sc[u][q] : mloc;
+      float mnew = kWide ? (float)ceil((double)mloc) : (float)mloc;
+      mnew = fmaxf(m[q], mnew);
+      if (mnew == FG_NEG_INF) continue;
+      const float corr = exp2f(m[q] - mnew);
+      l[q] *= corr;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[q][e] *= corr;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
         if (ok[u]) {
-          const float p = exp2f(s[u] - mnew);
+          const float p = exp2f((float)(sc[u][q] - (Score)mnew));
           float f[E];
           unpack16(vv[u], f, (const T*)nullptr);
-          l += p;
+          l[q] += p;
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = fmaf(p, f[e], acc[e]);
+          for (int e = 0; e < E; ++e) acc[q][e] = fmaf(p, f[e], acc[q][e]);
         }
       }
-      m = mnew;
+      m[q] = mnew;
     }
   }
-  // merge the lane groups of the warp
 #pragma unroll
-  for (int o = LPR; o < 32; o <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    float a2[E];
+  for (int q = 0; q < R; ++q) {
+    // merge the lane groups of the warp
 #pragma unroll
-    for (int e = 0; e < E; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
-    const float M = fmaxf(m, m2);
-    if (M != FG_NEG_INF) {
-      const float fa = exp2f(m - M), fb = exp2f(m2 - M);
-      l = l * fa + l2 * fb;
+    for (int o = LPR; o < 32; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[q], o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[q], o);
+      float a2[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * fa + a2[e] * fb;
-      m = M;
+      for (int e = 0; e < E; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[q][e], o);
+      const float M = fmaxf(m[q], m2);
+      if (M != FG_NEG_INF) {
+        const float fa = exp2f(m[q] - M), fb = exp2f(m2 - M);
+        l[q] = l[q] * fa + l2 * fb;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[q][e] = acc[q][e] * fa + a2[e] * fb;
+        m[q] = M;
+      }
     }
-  }
-  if (grp == 0) {
+    if (grp == 0) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) sm_acc[warp][gl * E + e] = acc[e];
-    if (gl == 0) {
-      sm_m[warp] = m;
-      sm_l[warp] = l;
+      for (int e = 0; e < E; ++e) sm_acc[q][warp][gl * E + e] = acc[q][e];
+      if (gl == 0) {
+        sm_m[q][warp] = m[q];
+        sm_l[q][warp] = l[q];
+      }
     }
   }
   __syncthreads();
   if (threadIdx.x < D) {
     const int t = threadIdx.x;
-    float M = FG_NEG_INF;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float L = 0.f, A = 0.f;
-    if (M != FG_NEG_INF) {
+    for (int q = 0; q < R; ++q) {
+      float M = FG_NEG_INF;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float f = exp2f(sm_m[w] - M);
-        L += sm_l[w] * f;
-        A += sm_acc[w][t] * f;
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[q][w]);
+      float L = 0.f, A = 0.f;
+      if (M != FG_NEG_INF) {
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          const float f = exp2f(sm_m[q][w] - M);
+          L += sm_l[q][w] * f;
+          A += sm_acc[q][w][t] * f;
+        }
       }
-    }
-    a.part_acc[(size_t)wi * D + t] = A;
-    if (t == 0) {
-      a.part_ml[2 * (size_t)wi] = M;
-      a.part_ml[2 * (size_t)wi + 1] = L;
+      const size_t slot = (size_t)wi * R + q;
+      a.part_acc[slot * D + t] = A;
+      if (t == 0) {
+        a.part_ml[2 * slot] = M;
+        a.part_ml[2 * slot + 1] = L;
+      }
     }
   }
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G, int HL) {
+__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G, int H, int R,
+                                                      int HLkv) {
   constexpr int PL = D / 32;
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x * 8 + warp;
+  const int g = blockIdx.x * 8 + warp;  // query head
   if (g >= G) return;
-  const fg_head_desc hd = a.desc[g];
+  const int c = kv_head(g, H, R), q = (g % H) % R;  // its cache and place in the group
+  const fg_head_desc hd = a.desc[c];
   const size_t w0 = (size_t)hd.work_off;
   // items in groups of 32: lane i holds item i's (max, sum); the weights are
   // then broadcast while every lane sums its PL dimensions over the items
   float M = FG_NEG_INF;
-  for (int i = lane; i < hd.n_work; i += 32) M = fmaxf(M, a.part_ml[2 * (w0 + i)]);
+  for (int i = lane; i < hd.n_work; i += 32) M = fmaxf(M, a.part_ml[2 * ((w0 + i) * R + q)]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f, acc[PL];
@@ -245,15 +280,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G,
       const int i = base + lane;
       float wgt = 0.f;
       if (i < hd.n_work) {
-        const float mi = a.part_ml[2 * (w0 + i)];
+        const size_t slot = (w0 + i) * R + q;
+        const float mi = a.part_ml[2 * slot];
         wgt = mi == FG_NEG_INF ? 0.f : exp2f(mi - M);
-        L += wgt * a.part_ml[2 * (w0 + i) + 1];
+        L += wgt * a.part_ml[2 * slot + 1];
       }
       const int cnt = min(32, hd.n_work - base);
 #pragma unroll 4
       for (int j = 0; j < cnt; ++j) {
         const float wj = __shfl_sync(0xffffffffu, wgt, j);
-        const float* pa = a.part_acc + (w0 + base + j) * D + lane * PL;
+        const float* pa = a.part_acc + ((w0 + base + j) * R + q) * D + lane * PL;
 #pragma unroll
         for (int e = 0; e < PL; ++e) acc[e] = fmaf(wj, pa[e], acc[e]);
       }
@@ -265,28 +301,38 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G,
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
   for (int e = 0; e < PL; ++e) store_out(out + lane * PL + e, acc[e] * inv);
-  if (lane == 0) {
-    const Placement pl = place(hd, a, HL, g);
-    if (pl.st) a.desc[g].n_static = hd.n_static + 1;
+  if (lane == 0 && q == 0) {  // one member advances the shared cache
+    const Placement pl = place(hd, a, HLkv, c);
+    if (pl.st) a.desc[c].n_static = hd.n_static + 1;
   }
 }
 
-// Both kernels are launched as programmatic dependents of the kernel before
-// them in the stream, hiding the launch gaps between decode steps.
-template <typename T, int D>
+template <typename T, int D, int R>
 cudaError_t run(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(split_kernel<T, D>, a.n_work, kDecThreads, 0, s, a, pd.HL, pd.sl2);
+  cudaError_t e = launch_pdl(split_kernel<T, D, R>, a.n_work, kDecThreads, 0, s, a, pd.H, pd.HLkv,
+                             pd.sl2);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, 0, s, a, pd.G, pd.HL);
+    e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, 0, s, a, pd.G, pd.H, pd.R, pd.HLkv);
   return e;
+}
+
+template <typename T, int D>
+cudaError_t run_r(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
+  switch (pd.R) {
+    case 1: return run<T, D, 1>(pd, a, s);
+    case 2: return run<T, D, 2>(pd, a, s);
+    case 4: return run<T, D, 4>(pd, a, s);
+    case 8: return run<T, D, 8>(pd, a, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
   if (pd.dtype == FG_FP32)
-    return pd.d == 64 ? run<float, 64>(pd, a, s) : run<float, 128>(pd, a, s);
-  return pd.d == 64 ? run<__nv_bfloat16, 64>(pd, a, s) : run<__nv_bfloat16, 128>(pd, a, s);
+    return pd.d == 64 ? run_r<float, 64>(pd, a, s) : run_r<float, 128>(pd, a, s);
+  return pd.d == 64 ? run_r<__nv_bfloat16, 64>(pd, a, s) : run_r<__nv_bfloat16, 128>(pd, a, s);
 }
 
 }  // namespace fg

@@ -13,9 +13,14 @@ constexpr int kRowsPerWork = 256;
 
 struct ProfileDims {
   int G, HL, B, n, d, dtype;
+  int H, Hkv, R;   // heads and key/value heads per layer; group size R = H / Hkv
+  int Gkv, HLkv;   // key/value head instances; L * Hkv
   int w, k;
   float T, sl2;  // sl2 = scale * log2(e): scores are kept in base-2 units
 };
+
+// Key/value head serving query head g.
+__host__ __device__ inline int kv_head(int g, int H, int R) { return (g / H) * (H / R) + (g % H) / R; }
 
 // Token class per prompt position: bit 0 special, bit 1 punctuation.  Also
 // zeroes the two work counters of the profiler passes (when non-null).
@@ -44,15 +49,22 @@ cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const floa
                           const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
                           uint8_t* keep, int32_t* kept, cudaStream_t s);
 
-cudaError_t launch_plan(int G, int w, int reserve, const int8_t* policy, const int32_t* cost,
-                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s);
+// Per key/value head c: the group policy (largest member policy) and the size
+// of the union of the members' never-evicted prompt sets, as int2 cinfo[c].
+cudaError_t launch_group(const ProfileDims& pd, const int8_t* policy, const uint8_t* keep,
+                         int2* cinfo, cudaStream_t s);
+
+// Writes one descriptor per cache from cinfo and builds the decode work list
+// (every cache gets at least one item).
+cudaError_t launch_plan(int Gkv, int w, int reserve, const int2* cinfo, fg_head_desc* desc,
+                        int2* work, long long* totals, cudaStream_t s);
 
 cudaError_t launch_compact(const ProfileDims& pd, const void* K, const void* V,
                            const uint8_t* keep, const fg_head_desc* desc, void* Kp, void* Vp,
                            int32_t* posp, cudaStream_t s);
 
 struct DecodeArgs {
-  fg_head_desc* desc;
+  fg_head_desc* desc;  // per cache (key/value head)
   const int2* work;
   int n_work;
   void* Kp;
@@ -68,8 +80,8 @@ struct DecodeArgs {
   int np;
   int pos;
   void* out;
-  float* part_ml;   // [n_work, 2]
-  float* part_acc;  // [n_work, d]
+  float* part_ml;   // [n_work, R, 2]
+  float* part_acc;  // [n_work, R, d]
   int32_t* dev_err;
 };
 

@@ -75,13 +75,13 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) lse_kernel(const T* __restrict__ Q,
                                                        const T* __restrict__ K,
                                                        float* __restrict__ lse2, int n,
-                                                       int ld, float sl2) {
+                                                       int ld, float sl2, int H, int R) {
   extern __shared__ float smem[];
   float* Qs = smem;
   float* Ks = smem + kTile * (D + 1);
   const int g = blockIdx.x, i0 = blockIdx.y * kTile;
   const T* Qg = Q + (size_t)g * n * D;
-  const T* Kg = K + (size_t)g * n * D;
+  const T* Kg = K + (size_t)kv_head(g, H, R) * n * D;  // the query head's key/value head
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   load_tile<T, D>(Qs, Qg, i0, n, sl2);
   float m[4], l[4];
@@ -134,14 +134,14 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const T* __restrict__ 
                                                           const float* __restrict__ lse2,
                                                           float* __restrict__ colsum,
                                                           float* __restrict__ bandcol, int n,
-                                                          int ld, int w, float sl2) {
+                                                          int ld, int w, float sl2, int H, int R) {
   extern __shared__ float smem[];
   float* Ks = smem;
   float* Qs = smem + kTile * (D + 1);
   float* Ls = Qs + kTile * (D + 1);
   const int g = blockIdx.x, j0 = blockIdx.y * kTile;
   const T* Qg = Q + (size_t)g * n * D;
-  const T* Kg = K + (size_t)g * n * D;
+  const T* Kg = K + (size_t)kv_head(g, H, R) * n * D;  // the query head's key/value head
   const float* Lg = lse2 + (size_t)g * ld;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   load_tile<T, D>(Ks, Kg, j0, n, 1.f);
@@ -191,9 +191,9 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2
   if (e != cudaSuccess) return e;
   dim3 grid(pd.G, cdiv(pd.n, kTile));
   lse_kernel<T, D><<<grid, kThreads, sm1, s>>>((const T*)Q, (const T*)K, lse2, pd.n, ld,
-                                               pd.sl2);
+                                               pd.sl2, pd.H, pd.R);
   colsum_kernel<T, D><<<grid, kThreads, sm2, s>>>((const T*)Q, (const T*)K, lse2, colsum,
-                                                  bandcol, pd.n, ld, pd.w, pd.sl2);
+                                                  bandcol, pd.n, ld, pd.w, pd.sl2, pd.H, pd.R);
   return cudaGetLastError();
 }
 

@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     profile_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, float* __restrict__ nlse2,
                       float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
-                      int ld, int nt, int w, float sl2, int32_t* __restrict__ sched,
-                      int32_t* __restrict__ err) {
+                      int ld, int nt, int w, float sl2, int H, int R,
+                      int32_t* __restrict__ sched, int32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& s = *reinterpret_cast<TcSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -290,8 +290,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // the operand loaded per unit may be replaced once the previous
         // unit's MMAs are done with it
         if (ucount >= 1 && !wait_or_abort(&s.a_empty, (ucount - 1) & 1, abort)) break;
+        // Q rows come from query head g, K rows from its key/value head
+        const int gk = kv_head(g, H, R);
         mbar_expect_tx(&s.a_full, TileCfg<D>::kTileBytes);
-        load_tile<D>(s.a, mapA, &s.a_full, um.at * kBlk, g);
+        load_tile<D>(s.a, mapA, &s.a_full, um.at * kBlk, PASS == 1 ? g : gk);
         bool stop = false;
         for (int t = 0; t < um.nb; ++t) {
           const int st = bseq % kStages;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           mbar_expect_tx(&s.full[st], TileCfg<D>::kTileBytes);
-          load_tile<D>(s.b[st], mapB, &s.full[st], (um.b_first + t) * kBlk, g);
+          load_tile<D>(s.b[st], mapB, &s.full[st], (um.b_first + t) * kBlk, PASS == 1 ? gk : g);
           ++bseq;
           if (PASS == 2) {
             const int ls = lseq % kLseSlots;
@@ -510,7 +512,7 @@ template <int D>
 cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse2, int ld,
                 float* colsum, float* bandcol, int32_t* sched, int32_t* err, cudaStream_t s) {
   CUtensorMap tq, tk;
-  if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.G, pd.n, D))
+  if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.Gkv, pd.n, D))
     return cudaErrorInvalidValue;
   const int nt = cdiv(pd.n, kBlk);
   const size_t smem = sizeof(TcSmem<D>) + 1024;
@@ -526,10 +528,10 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
   const unsigned grid = (unsigned)(units < 2LL * sms ? units : 2LL * sms);
   // the work counters were zeroed by the token-class kernel launched before
   e = launch_pdl(profile_tc_kernel<1, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum, bandcol,
-                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, sched, err);
+                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, sched, err);
   if (e == cudaSuccess)
     e = launch_pdl(profile_tc_kernel<2, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum,
-                   bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, sched + 1, err);
+                   bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, sched + 1, err);
   return e;
 }
 

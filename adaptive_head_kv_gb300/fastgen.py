@@ -37,7 +37,7 @@ class Params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("L", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("n", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("T", ctypes.c_float), ("r_l", ctypes.c_float), ("r_f", ctypes.c_float),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("Hkv", ctypes.c_int32)]
 
 
 class HeadDesc(ctypes.Structure):
@@ -156,9 +156,9 @@ def fastgen_plan_bytes(params: Params, max_new_tokens: int) -> int:
     return lib().fastgen_plan_bytes(ctypes.byref(params), max_new_tokens)
 
 
-def fastgen_compact_plan(params, policy, cost, max_new_tokens, plan, stream=None) -> PlanInfo:
+def fastgen_compact_plan(params, policy, keep, max_new_tokens, plan, stream=None) -> PlanInfo:
     info = PlanInfo()
-    _check(lib().fastgen_compact_plan(ctypes.byref(params), _ptr(policy), _ptr(cost),
+    _check(lib().fastgen_compact_plan(ctypes.byref(params), _ptr(policy), _ptr(keep),
                                       max_new_tokens, _ptr(plan), plan.numel() * plan.element_size(),
                                       ctypes.byref(info), _stream(stream)), "fastgen_compact_plan")
     return info

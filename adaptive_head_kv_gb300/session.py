@@ -11,10 +11,10 @@ import torch
 from . import fastgen as fg
 
 
-def make_params(B, L, H, n, d, dtype, T, r_l, r_f, scale=0.0) -> fg.Params:
+def make_params(B, L, H, n, d, dtype, T, r_l, r_f, scale=0.0, Hkv=0) -> fg.Params:
     code = {"bf16": fg.FG_BF16, "fp32": fg.FG_FP32, torch.bfloat16: fg.FG_BF16,
             torch.float32: fg.FG_FP32}[dtype]
-    return fg.Params(B, L, H, n, d, code, T, r_l, r_f, scale)
+    return fg.Params(B, L, H, n, d, code, T, r_l, r_f, scale, Hkv)
 
 
 GUARD_BYTES = 4096
@@ -36,6 +36,7 @@ class FastGenSession:
         self._guards = []
         G, n = params.B * params.L * params.H, params.n
         self.G = G
+        self.Gkv = params.B * params.L * (params.Hkv or params.H)  # caches (key/value heads)
         self.tdtype = torch.bfloat16 if params.dtype == fg.FG_BF16 else torch.float32
         dev = self.device
         self.special = torch.as_tensor(special_ids, dtype=torch.int32, device=dev)
@@ -62,7 +63,7 @@ class FastGenSession:
                            self.dev_err, self.stream)
 
     def compact(self, K, V):
-        self.info = fg.fastgen_compact_plan(self.p, self.policy, self.cost, self.max_new,
+        self.info = fg.fastgen_compact_plan(self.p, self.policy, self.keep, self.max_new,
                                             self.plan, self.stream)
         rows = int(self.info.pool_rows)
         if self.pos_pool is None or self.pos_pool.numel() < rows:
@@ -81,6 +82,8 @@ class FastGenSession:
         self.compact(K, V)
 
     def decode(self, q, k_new, v_new, new_ids, pos, out=None):
+        """One generation step: q [G, d] per query head, k_new/v_new [Gkv, d]
+        per key/value head, new_ids [B]; returns out [G, d]."""
         out = self.out if out is None else out
         fg.fastgen_decode_attn(self.p, self.plan, self.info, self.K_pool, self.V_pool,
                                self.pos_pool, q, k_new, v_new, new_ids, self.special, self.punct,
@@ -88,8 +91,8 @@ class FastGenSession:
         return out
 
     def capture_decode(self, q, k, v, new_ids, pos0):
-        """Captures len(q) consecutive decode calls (inputs q, k, v
-        [steps, G, d] and new_ids [steps, B] on the device, positions pos0,
+        """Captures len(q) consecutive decode calls (inputs q [steps, G, d],
+        k, v [steps, Gkv, d] and new_ids [steps, B] on the device, positions pos0,
         pos0 + 1, ...) as one CUDA graph; returns (graph, outs [steps, G, d]).
         Replaying it runs those steps on the session's current caches.  The
         plan and pools must not be reallocated between replays."""
@@ -123,8 +126,8 @@ class FastGenSession:
         return bad
 
     def descriptors(self):
-        """Host copy of the per-head descriptors (for inspection and tests)."""
+        """Host copy of the per-cache descriptors (for inspection and tests)."""
         import ctypes
 
-        raw = self.plan[: self.G * ctypes.sizeof(fg.HeadDesc)].cpu().numpy().tobytes()
-        return (fg.HeadDesc * self.G).from_buffer_copy(raw)
+        raw = self.plan[: self.Gkv * ctypes.sizeof(fg.HeadDesc)].cpu().numpy().tobytes()
+        return (fg.HeadDesc * self.Gkv).from_buffer_copy(raw)

@@ -16,7 +16,11 @@
  * fastgen_decode_attn (one generation step for every head).
  *
  * Conventions shared by every entry point
- *   - Heads are a flat index g = (b*L + l)*H + h over G = B*L*H instances.
+ *   - Query heads are a flat index g = (b*L + l)*H + h over G = B*L*H
+ *     instances.  Keys and values have Hkv heads per layer (grouped-query
+ *     attention when Hkv < H): key/value head c = (b*L + l)*Hkv + h / (H/Hkv)
+ *     serves query head g, over Gkv = B*L*Hkv instances.  Each key/value head
+ *     keeps one compressed cache, shared by the query heads of its group.
  *   - All array arguments are DEVICE pointers owned by the caller unless
  *     marked HOST; the library never allocates, frees or keeps memory
  *     between calls, and has no global state.  Scratch memory is passed in
@@ -77,9 +81,11 @@ typedef struct {
   float r_l;       /* local ratio in [0, 1]: window w = ceil(r_l * n) */
   float r_f;       /* frequent ratio in [0, 1]: k = ceil(r_f * n) keys */
   float scale;     /* score scale s in softmax(s Q K^T); 0 selects 1/sqrt(d) */
+  int32_t Hkv;     /* key/value heads per layer; 0 selects H (no grouping).  H must be
+                      a multiple of Hkv with a group size H/Hkv of 1, 2, 4 or 8. */
 } fg_params;
 
-/* One head's compressed cache inside the pooled K/V buffers. */
+/* One key/value head's compressed cache inside the pooled K/V buffers. */
 typedef struct {
   int64_t off;        /* first pool row of the never-evicted segment */
   int32_t n_static;   /* rows currently used in that segment */
@@ -124,8 +130,11 @@ int32_t fastgen_version(void);
  *   kept[g]   = cost[g, policy[g]].
  * Ratios are evaluated as ceil(r * n) exactly on the float value of r.
  *
+ * With groups, every query head is profiled on its own against its group's
+ * keys (the per-head outputs below are per query head).
+ *
  * Arguments:
- *   Q, K        [G, n, d] dtype, row-major, 16-byte aligned.
+ *   Q [G, n, d] and K [Gkv, n, d], dtype, row-major, 16-byte aligned.
  *   token_ids   [B, n] int32 prompt token ids.
  *   special_ids [n_special] int32, punct_ids [n_punct] int32 (0 <= counts <= 4096;
  *               a count of 0 allows a NULL pointer).
@@ -152,24 +161,27 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
 /* ------------------------------------------------------------------------
  * Compaction, step 1: the pool layout (Method: K_C, V_C = f(K, V, C)).
  *
- * From policy [G] and cost [G,5] (outputs of fastgen_profile) it writes, into
- * the device buffer `plan` (>= fastgen_plan_bytes bytes, 256-byte aligned):
- * G fg_head_desc records followed by the decode work list.  Each head gets a
- * never-evicted segment of (kept static rows + max_new_tokens) rows and, for
- * SPFL heads, a ring of w rows for the sliding window.  The totals are
- * written to *info (HOST pointer).  This call is SYNCHRONOUS: it waits on
- * `stream` to return the totals.
+ * From policy [G] and keep [G, n] (outputs of fastgen_profile) it writes,
+ * into the device buffer `plan` (>= fastgen_plan_bytes bytes, 256-byte
+ * aligned): Gkv fg_head_desc records followed by the decode work list.  The
+ * cache of key/value head c holds the union of its query heads' caches (a
+ * position is never-evicted if any member keeps it so, else in the window if
+ * any member's window holds it) and follows the largest member policy; without
+ * groups that is the head's own cache.  Each cache gets a never-evicted
+ * segment of (kept static rows + max_new_tokens) rows and, for SPFL, a ring
+ * of w rows for the sliding window.  The totals are written to *info (HOST
+ * pointer).  This call is SYNCHRONOUS: it waits on `stream` to return them.
  * ------------------------------------------------------------------------ */
 size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens);
 
-fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const int32_t* cost,
+fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const uint8_t* keep,
                                int32_t max_new_tokens, void* plan, size_t plan_bytes,
                                fg_plan_info* info, void* stream);
 
 /* ------------------------------------------------------------------------
  * Compaction, step 2: gather the kept prompt rows into the pools.
  *
- * K, V [G, n, d] dtype; keep [G, n] from fastgen_profile; plan and *info
+ * K, V [Gkv, n, d] dtype; keep [G, n] from fastgen_profile; plan and *info
  * (HOST pointer) from fastgen_compact_plan.  Writes K_pool, V_pool
  * [pool_rows, d] dtype and pos_pool [pool_rows] int32 (absolute position of
  * each row, -1 = empty).  Never-evicted rows are stored in position order;
@@ -194,8 +206,9 @@ fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, cons
  * over the cache after placement.
  *
  * Arguments: plan and *info (HOST pointer) from fastgen_compact_plan; pools
- * from fastgen_compact (updated in place); q, k_new, v_new [G, d] dtype;
- * new_ids [B] int32; id sets as in fastgen_profile; out [G, d] dtype;
+ * from fastgen_compact (updated in place); q [G, d], k_new, v_new [Gkv, d]
+ * dtype; new_ids [B] int32; id sets as in fastgen_profile; out [G, d] dtype
+ * (every query head attends over its group's cache);
  * workspace >= fastgen_decode_workspace_bytes(p, info).  dev_err: device
  * int32 that the call ORs with 1 when a head had no free reserved row (that
  * token is then not stored); read it with fastgen_read_error.

@@ -39,12 +39,14 @@ def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True, guard=True):
     w = make_workload(cfg, seed)
     n, steps = cfg.n, cfg.steps
     dev = torch.device("cuda")
+    sel = kv_rows(cfg)  # the workload lists K/V per query head: one row per cache
     Q = w["Q"][:, :n].contiguous().to(dev)
-    K = w["K"][:, :n].contiguous().to(dev)
-    V = w["V"][:, :n].contiguous().to(dev)
+    K = w["K"][sel, :n].contiguous().to(dev)
+    V = w["V"][sel, :n].contiguous().to(dev)
     ids = torch.from_numpy(w["ids"]).to(dev)
     T = cfg.T if T is None else T
-    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, T, cfg.r_l, cfg.r_f)
+    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, T, cfg.r_l, cfg.r_f,
+                    Hkv=cfg.Hkv)
     s = FastGenSession(p, special_ids(seed), punct_ids(seed),
                        cfg.steps if max_new is None else max_new, guard=guard)
     s.prefill(Q, K, V, ids[:, :n].contiguous())
@@ -59,8 +61,8 @@ def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True, guard=True):
         res["Kp0"] = s.K_pool.cpu()
         res["Vp0"] = s.V_pool.cpu()
     Qd = w["Q"][:, n:].transpose(0, 1).contiguous().to(dev)
-    Kd = w["K"][:, n:].transpose(0, 1).contiguous().to(dev)
-    Vd = w["V"][:, n:].transpose(0, 1).contiguous().to(dev)
+    Kd = w["K"][sel, n:].transpose(0, 1).contiguous().to(dev)
+    Vd = w["V"][sel, n:].transpose(0, 1).contiguous().to(dev)
     idd = ids[:, n:].transpose(0, 1).contiguous()
     outs = torch.empty(steps, s.G, cfg.d, dtype=s.tdtype, device=dev)
     for st in range(steps):
@@ -73,6 +75,12 @@ def run_gpu(cfg, seed=0, max_new=None, T=None, check_pools=True, guard=True):
     res["pos1"] = s.pos_pool.cpu().numpy()
     res["session"] = s
     return res
+
+
+def kv_rows(cfg):
+    """For each cache (key/value head), the first query head of its group."""
+    r = cfg.H // cfg.kv_heads
+    return [(c // cfg.kv_heads) * cfg.H + (c % cfg.kv_heads) * r for c in range(cfg.Gkv)]
 
 
 def oracle_head(cfg, w, idx, T=None):
@@ -212,3 +220,50 @@ def sample_heads(cfg, types, count, seed=1):
     while len(pick) < min(count, G):
         pick.add(int(rng.integers(0, G)))
     return sorted(pick)
+
+
+def compare_groups(cfg, gpu, T=None):
+    """Grouped-query parity: every query head's profile as in compare(), and
+    for each cache the union of its members' caches, the group policy, the
+    compacted rows and every member's decode outputs (oracle decode_group).
+    A group with an exempt member is checked for its members' profiles only."""
+    w = gpu["workload"]
+    T = float(np.float32(cfg.T if T is None else T))
+    n, r = cfg.n, cfg.H // cfg.kv_heads
+    rep = dict(groups=0, groups_exempt=0)
+    compare(cfg, gpu, [], T=T)  # all-head invariants, guards
+    for c, g0 in enumerate(kv_rows(cfg)):
+        members = list(range(g0, g0 + r))
+        b = g0 // (cfg.L * cfg.H)
+        Qs = [w["Q"][g].double().numpy() for g in members]
+        Ka = w["K"][g0].double().numpy()
+        Va = w["V"][g0].double().numpy()
+        ids = w["ids"][b]
+        res, keep, pol = O.profile_group([q[:n] for q in Qs], Ka[:n], ids, special_ids(),
+                                         punct_ids(), T, cfg.r_l, cfg.r_f)
+        exempt = False
+        for g, ora in zip(members, res):
+            assert close(gpu["colsum"][g], ora["colsum"], RTOL, COLSUM_ATOL).all(), g
+            assert close(gpu["mass"][g], ora["mass"], RTOL, MASS_ATOL).all(), g
+            if policy_exempt(ora, T) or (topk_exempt(ora) and ora["policy"] in (2, 3)):
+                exempt = True
+                continue
+            assert gpu["policy"][g] == ora["policy"], (g, gpu["policy"][g], ora["policy"])
+            assert np.array_equal(gpu["keep"][g], ora["keep"]), g
+        rep["groups"] += 1
+        if exempt:
+            rep["groups_exempt"] += 1
+            continue
+        d0 = gpu["desc0"][c]
+        sp = np.nonzero(keep == O.KEEP_STATIC)[0]
+        assert d0.policy == pol and d0.n_static == len(sp), (c, d0.policy, pol)
+        assert np.array_equal(gpu["pos0"][d0.off: d0.off + len(sp)], sp), c
+        assert torch.equal(gpu["Kp0"][d0.off: d0.off + len(sp)], w["K"][g0][sp])
+        wl = res[0]["w"]
+        out, pos = O.decode_group(pol, keep, n, wl, ids, Qs, Ka, Va, special_ids(), punct_ids(),
+                                  cfg.steps)
+        for mi, g in enumerate(members):
+            err = np.abs(gpu["out"][:, g] - out[mi]).max()
+            assert err <= dec_atol(cfg.dtype), (c, g, err)
+        assert np.array_equal(cache_positions(gpu["desc1"][c], gpu["pos1"]), pos), c
+    return rep

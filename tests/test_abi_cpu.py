@@ -42,7 +42,7 @@ def test_header_symbols_exported():
 
 
 def test_struct_sizes():
-    assert ctypes.sizeof(fg.Params) == 40
+    assert ctypes.sizeof(fg.Params) == 44
     assert ctypes.sizeof(fg.HeadDesc) == 40
     assert ctypes.sizeof(fg.PlanInfo) == 16
 
@@ -55,7 +55,8 @@ def test_status_strings_and_version():
 
 
 def P(**kw):
-    base = dict(B=1, L=2, H=3, n=100, d=128, dtype=fg.FG_BF16, T=0.95, r_l=0.3, r_f=0.3, scale=0.0)
+    base = dict(B=1, L=2, H=3, n=100, d=128, dtype=fg.FG_BF16, T=0.95, r_l=0.3, r_f=0.3, scale=0.0,
+                Hkv=0)
     base.update(kw)
     return fg.Params(**base)
 
@@ -67,7 +68,7 @@ def test_workspace_sizes():
     assert fg.fastgen_profile_workspace_bytes(p) == al(G * 128 * 4) + al(G * n * 4) + al(n) + 256
     w = 30
     work = G * ((n + 7 + 255) // 256 + (w + 255) // 256)
-    assert fg.fastgen_plan_bytes(p, 7) == al(G * 40) + 256 + work * 8
+    assert fg.fastgen_plan_bytes(p, 7) == al(G * 40) + al(G * 8) + 256 + work * 8
     info = fg.PlanInfo(1000, 13, 256)
     assert fg.fastgen_decode_workspace_bytes(p, info) == al(13 * 8) + al(13 * 128 * 4)
     assert fg.fastgen_profile_workspace_bytes(P(d=96)) == 0
@@ -91,6 +92,8 @@ def profile_status(p, ws_bytes=1 << 40, ptrs=None, ns=1, np_=1):
     (dict(r_l=-0.1), fg.FG_EINVAL), (dict(r_f=1.01), fg.FG_EINVAL), (dict(n=0), fg.FG_EINVAL),
     (dict(B=0), fg.FG_EINVAL), (dict(d=96), fg.FG_EDTYPE), (dict(dtype=7), fg.FG_EDTYPE),
     (dict(scale=-1.0), fg.FG_EINVAL), (dict(scale=float("inf")), fg.FG_EINVAL),
+    (dict(Hkv=2), fg.FG_EINVAL), (dict(Hkv=-1), fg.FG_EINVAL),
+    (dict(H=48, Hkv=4), fg.FG_EDTYPE),  # group size 12 is not supported
 ])
 def test_profile_rejects_bad_params(kw, status):
     assert profile_status(P(**kw)) == status
@@ -139,3 +142,16 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(fg, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(FileNotFoundError):
         fg.fastgen_version()
+
+
+def test_group_sizes_in_buffer_sizes():
+    """With key/value groups the plan has one descriptor per key/value head
+    and the decode workspace one partial per item and query head."""
+    al = lambda x: (x + 255) // 256 * 256
+    p = P(H=8, Hkv=2, n=100)
+    Gkv = 1 * 2 * 2
+    w = 30
+    work = Gkv * ((100 + 7 + 255) // 256 + (w + 255) // 256)
+    assert fg.fastgen_plan_bytes(p, 7) == al(Gkv * 40) + al(Gkv * 8) + 256 + work * 8
+    info = fg.PlanInfo(1000, 13, 256)
+    assert fg.fastgen_decode_workspace_bytes(p, info) == al(13 * 4 * 8) + al(13 * 4 * 128 * 4)
