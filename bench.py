@@ -161,24 +161,38 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def group_caches(cfg, policy, keep):
+    """Per cache (key/value head): the group policy (largest member policy)
+    and the union of the members' keep codes; without groups, the heads'."""
+    r = cfg.H // cfg.kv_heads
+    if r == 1:
+        return policy, keep
+    pol = policy.reshape(-1, r).max(axis=1)
+    k = keep.reshape(-1, r, keep.shape[1])
+    static = (k == 1).any(axis=1)
+    window = (k == 2).any(axis=1)
+    return pol, np.where(static, 1, np.where(window, 2, 0)).astype(np.uint8)
+
+
 def cache_rows_per_step(cfg, policy, keep, ids, special, punct):
-    """Rows each generation step attends over, summed over heads (bookkeeping
-    for the roofline's algorithmic bytes; follows the documented placement
-    rule from the profile's outputs)."""
-    n, steps, G, HL = cfg.n, cfg.steps, cfg.G, cfg.L * cfg.H
+    """Rows each generation step attends over, summed over caches
+    (bookkeeping for the roofline's algorithmic bytes; follows the documented
+    placement rule from the profile's outputs).  policy/keep: per cache."""
+    n, steps = cfg.n, cfg.steps
+    C, HL = keep.shape[0], cfg.L * cfg.kv_heads
     w = int(np.ceil(float(np.float32(cfg.r_l)) * n))
-    b_of = np.arange(G) // HL
+    b_of = np.arange(C) // HL
     dec = ids[:, n:n + steps]
     is_s = np.isin(dec, special)
     is_p = np.isin(dec, punct)
     pol = policy.astype(np.int64)[:, None]
     st = np.where(pol == 4, True, np.where(pol == 0, is_s[b_of], (is_s | is_p)[b_of]))
     n_static0 = (keep == 1).sum(axis=1)
-    static_t = n_static0[:, None] + np.cumsum(st, axis=1)  # [G, steps]
-    ring_ind = np.zeros((G, n + steps), dtype=np.int64)
+    static_t = n_static0[:, None] + np.cumsum(st, axis=1)  # [C, steps]
+    ring_ind = np.zeros((C, n + steps), dtype=np.int64)
     ring_ind[:, :n] = keep == 2
     ring_ind[:, n:] = (pol == 3) & ~st & (w > 0)
-    csum = np.concatenate([np.zeros((G, 1), np.int64), np.cumsum(ring_ind, axis=1)], axis=1)
+    csum = np.concatenate([np.zeros((C, 1), np.int64), np.cumsum(ring_ind, axis=1)], axis=1)
     t = np.arange(n, n + steps)
     lo = np.maximum(t - w + 1, 0)
     ring_t = csum[:, t + 1] - csum[:, lo]
@@ -206,7 +220,7 @@ def run_ours(args, cfg, rank, world):
     Q, K, V = hQ.to(dev), hK.to(dev), hV.to(dev)
     q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
     ids, dec_ids = hids.to(dev), hdec_ids.to(dev)
-    p = make_params(cfg.B, cfg.L, cfg.H, n, d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    p = make_params(cfg.B, cfg.L, cfg.H, n, d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f, Hkv=cfg.Hkv)
     s = FastGenSession(p, special_ids(rank), punct_ids(rank), steps, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -263,18 +277,23 @@ def run_ours(args, cfg, rank, world):
     # algorithmic work
     policy = s.policy.cpu().numpy()
     keep = s.keep.cpu().numpy()
-    rows_t, ring_t = cache_rows_per_step(cfg, policy, keep, ids_np, special_ids(rank),
+    cpol, ckeep = group_caches(cfg, policy, keep)
+    rows_t, ring_t = cache_rows_per_step(cfg, cpol, ckeep, ids_np, special_ids(rank),
                                          punct_ids(rank))
     eb = 2 if cfg.dtype == "bf16" else 4
-    dec_bytes_t = rows_t * d * 2 * eb + G * d * eb * 4 + ring_t * 4 + G * 40
+    Gkv = cfg.Gkv
+    # K/V rows of every cache + q and out per query head + k_new, v_new per
+    # cache + ring positions + descriptors
+    dec_bytes_t = (rows_t * d * 2 * eb + G * d * eb * 2 + Gkv * d * eb * 2 + ring_t * 4
+                   + Gkv * 40)
     dec_gbs = dec_bytes_t.sum() / (dec_ms.sum() * 1e-3) / 1e9
     prof_flops = 2.0 * n * (n + 1) * d * G
-    kept_rows = int((keep != 0).sum())
-    comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + G * 40
+    kept_rows = int((ckeep != 0).sum())
+    comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + Gkv * 40
     return dict(cfg=cfg, prof_ms=prof_ms, comp_ms=comp_ms, decode_ms=decode_ms, step_ms=step_ms,
                 total_ms=total_ms, dec_ms=dec_ms, dec_bytes=float(dec_bytes_t.mean()),
                 dec_gbs=dec_gbs, prof_flops=prof_flops, comp_bytes=comp_bytes,
-                kept_frac=kept_rows / (G * n), clocks=clk.summary(),
+                kept_frac=kept_rows / (Gkv * n), clocks=clk.summary(),
                 e2e=run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream))
 
 
@@ -289,7 +308,8 @@ def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
     hout = torch.empty(steps, s.G, cfg.d, dtype=s.tdtype).pin_memory()
     Q, K, V = (torch.empty_like(x, device=dev) for x in (hQ, hK, hV))
     ids = torch.empty_like(hids, device=dev)
-    qs, ks, vs = (torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev) for _ in range(3))
+    qs = torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev)
+    ks, vs = (torch.empty(s.Gkv, cfg.d, dtype=s.tdtype, device=dev) for _ in range(2))
     did = torch.empty(cfg.B, dtype=torch.int32, device=dev)
 
     def step():
@@ -316,12 +336,12 @@ def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     pre, dec = zip(*[step() for _ in range(max(1, min(args.steps, 3)))])
-    eb = hQ.element_size()
+    nb = lambda t: t.numel() * t.element_size()
     return dict(prefill_ms=float(np.mean(pre)), decode_ms=float(np.mean(dec)),
-                h2d=3 * hQ.numel() * eb + hids.numel() * 4,
-                d2h=s.G,
-                dec_h2d=steps * (3 * s.G * cfg.d * eb + cfg.B * 4),
-                dec_d2h=steps * s.G * cfg.d * eb)
+                h2d=nb(hQ) + nb(hK) + nb(hV) + nb(hids),
+                d2h=nb(hpol),
+                dec_h2d=nb(hq) + nb(hk) + nb(hv) + nb(hdec_ids),
+                dec_d2h=nb(hout))
 
 
 def oracle_sample(cfg, heads, seed=0):
@@ -382,6 +402,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=float, default=None, help="override the recover ratio")
+    ap.add_argument("--hkv", type=int, default=0,
+                    help="key/value heads per layer (grouped-query attention); 0 = H")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every decode call from the host instead of one CUDA graph")
     ap.add_argument("--layers", type=int, default=0,
@@ -400,6 +422,8 @@ def main():
         cfg = cfg.with_(L=args.layers, name=f"{cfg.name}_L{args.layers}")
     if args.T is not None:
         cfg = cfg.with_(T=args.T, name=f"{cfg.name}_T{args.T:g}")
+    if args.hkv:
+        cfg = cfg.with_(Hkv=args.hkv, name=f"{cfg.name}_kv{args.hkv}")
     if args.record_traffic:
         record_traffic(args.record_traffic, cfg.name, args.traffic_command)
         return
@@ -441,8 +465,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded generator, planted head types; no weights or datasets)",
-        "config": {"workload": f"{cfg.name}: B={cfg.B} L={cfg.L} H={cfg.H} d={cfg.d} n={cfg.n} "
-                               f"decode_steps={cfg.steps} T={cfg.T} r_l={cfg.r_l} r_f={cfg.r_f}",
+        "config": {"workload": f"{cfg.name}: B={cfg.B} L={cfg.L} H={cfg.H} Hkv={cfg.kv_heads} "
+                               f"d={cfg.d} n={cfg.n} decode_steps={cfg.steps} T={cfg.T} "
+                               f"r_l={cfg.r_l} r_f={cfg.r_f}",
                    "G": cfg.G, "parallelism": f"replicas x{world}",
                    "l2": "inputs and caches larger than L2 (no flush)",
                    "step": "profile + plan + compact + all decode steps",

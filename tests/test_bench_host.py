@@ -29,3 +29,13 @@ def test_cache_rows_match_oracle():
                                            special_ids(), punct_ids())
     assert np.array_equal(rows, sizes)
     assert (ring >= 0).all()
+
+
+def test_group_caches_union():
+    cfg = CONFIGS["tiny"].with_(L=1, H=4, Hkv=2, n=5)
+    policy = np.array([0, 3, 1, 2])
+    keep = np.array([[1, 0, 0, 0, 0], [1, 1, 0, 2, 2], [1, 0, 1, 0, 0], [0, 1, 1, 0, 0]],
+                    dtype=np.uint8)
+    pol, k = bench.group_caches(cfg, policy, keep)
+    assert list(pol) == [3, 2]
+    assert k.tolist() == [[1, 1, 0, 2, 2], [1, 1, 1, 0, 0]]
