@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
   constexpr int LPR = D / E;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp per load
   constexpr int STEP = kDecWarps * RPW;
-  constexpr int U = R == 1 ? 4 : (R == 2 ? 2 : 1);
+  constexpr int U = R <= 2 ? 4 : 2;
   constexpr bool kWide = sizeof(T) == 4;  // fp32 inputs: fp64 dot, scaled once
   using Score = typename std::conditional<kWide, double, float>::type;
   __shared__ float sm_m[R][kDecWarps], sm_l[R][kDecWarps];
