@@ -81,6 +81,30 @@ class FastGenSession:
         self.profile(Q, K, token_ids)
         self.compact(K, V)
 
+    def prefill_host(self, hQ, hK, hV, htoken_ids, Q, K, V, token_ids):
+        """prefill() from pinned host tensors: each of Q, K, V (and the ids)
+        is copied into its device buffer on its own stream, so the copies run
+        concurrently and the V copy overlaps the profiling."""
+        main = torch.cuda.current_stream(self.device)
+        if not hasattr(self, "_copy_streams"):
+            self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(3)]
+        done = []
+        for st, (dst, src) in zip(self._copy_streams,
+                                  ((Q, hQ), (K, hK), (V, hV))):
+            st.wait_stream(main)  # the buffers are free once earlier work is done
+            with torch.cuda.stream(st):
+                dst.copy_(src, non_blocking=True)
+                if dst is Q:
+                    token_ids.copy_(htoken_ids, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(st)
+            done.append(ev)
+        main.wait_event(done[0])
+        main.wait_event(done[1])
+        self.profile(Q, K, token_ids)
+        main.wait_event(done[2])
+        self.compact(K, V)
+
     def decode(self, q, k_new, v_new, new_ids, pos, out=None):
         """One generation step: q [G, d] per query head, k_new/v_new [Gkv, d]
         per key/value head, new_ids [B]; returns out [G, d]."""

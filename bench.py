@@ -308,27 +308,49 @@ def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
     hout = torch.empty(steps, s.G, cfg.d, dtype=s.tdtype).pin_memory()
     Q, K, V = (torch.empty_like(x, device=dev) for x in (hQ, hK, hV))
     ids = torch.empty_like(hids, device=dev)
-    qs = torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev)
-    ks, vs = (torch.empty(s.Gkv, cfg.d, dtype=s.tdtype, device=dev) for _ in range(2))
-    did = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+    # per-step inputs and outputs are double-buffered: the copies of step t+1
+    # and the read-back of step t-1 overlap the decode of step t
+    bufs = [(torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev),
+             torch.empty(s.Gkv, cfg.d, dtype=s.tdtype, device=dev),
+             torch.empty(s.Gkv, cfg.d, dtype=s.tdtype, device=dev),
+             torch.empty(cfg.B, dtype=torch.int32, device=dev),
+             torch.empty(s.G, cfg.d, dtype=s.tdtype, device=dev)) for _ in range(2)]
+    cp_in, cp_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step():
         a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         a.record(stream)
-        Q.copy_(hQ, non_blocking=True)
-        K.copy_(hK, non_blocking=True)
-        V.copy_(hV, non_blocking=True)
-        ids.copy_(hids, non_blocking=True)
-        s.prefill(Q, K, V, ids)
+        s.prefill_host(hQ, hK, hV, hids, Q, K, V, ids)
         hpol.copy_(s.policy, non_blocking=True)
         b.record(stream)
+        ready = [torch.cuda.Event(), torch.cuda.Event()]
+        used = [torch.cuda.Event(), torch.cuda.Event()]
+        read = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def stage(st, i):
+            if st >= 2:  # buffer i is free once the decode of step st - 2 has read it
+                cp_in.wait_event(used[i])
+            with torch.cuda.stream(cp_in):
+                for dst, src in zip(bufs[i][:4], (hq[st], hk[st], hv[st], hdec_ids[st])):
+                    dst.copy_(src, non_blocking=True)
+                ready[i].record(cp_in)
+
+        stage(0, 0)
         for st in range(steps):
-            qs.copy_(hq[st], non_blocking=True)
-            ks.copy_(hk[st], non_blocking=True)
-            vs.copy_(hv[st], non_blocking=True)
-            did.copy_(hdec_ids[st], non_blocking=True)
-            s.decode(qs, ks, vs, did, n + st)
-            hout[st].copy_(s.out, non_blocking=True)
+            i = st % 2
+            if st + 1 < steps:
+                stage(st + 1, 1 - i)
+            stream.wait_event(ready[i])
+            if st >= 2:
+                stream.wait_event(read[i])  # the output buffer has been read back
+            qb, kb, vb, ib, ob = bufs[i]
+            s.decode(qb, kb, vb, ib, n + st, out=ob)
+            used[i].record(stream)
+            cp_out.wait_event(used[i])
+            with torch.cuda.stream(cp_out):
+                hout[st].copy_(ob, non_blocking=True)
+                read[i].record(cp_out)
+        stream.wait_stream(cp_out)
         c.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b), b.elapsed_time(c)
