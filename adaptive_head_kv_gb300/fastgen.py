@@ -20,7 +20,7 @@ FG_POLICY_S, FG_POLICY_SP, FG_POLICY_SPF, FG_POLICY_SPFL, FG_POLICY_FULL = range
 FG_KEEP_DROP, FG_KEEP_STATIC, FG_KEEP_WINDOW = 0, 1, 2
 
 # kernels launched by one call of each entry point (counted in the bench)
-LAUNCHES = {"profile": 4, "plan": 2, "compact": 1, "decode": 2}
+LAUNCHES = {"profile": 4, "plan": 3, "compact": 1, "decode": 2}
 
 EXPORTS = (
     "fastgen_status_string", "fastgen_version", "fastgen_profile_workspace_bytes",

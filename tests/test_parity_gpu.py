@@ -165,3 +165,50 @@ def test_decode_graph_replay_matches_host_loop():
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(outs.float().cpu().numpy(), gpu["out"])
+
+
+
+class _HeadColumns:
+    """Decode outputs left on the device, read back one query head at a time."""
+
+    def __init__(self, outs):
+        self.outs = outs
+
+    def __getitem__(self, key):
+        _, g = key
+        return self.outs[:, g].float().cpu().numpy().astype(np.float64)
+
+
+def test_llama65b_full_size_sampled():
+    """The largest workload at full size (G = 40960 heads, n = 2048, 1024
+    decode steps, CUDA-graph decode as the benchmark runs it): every head's
+    invariants, then sampled heads of every type, first and last layer,
+    against the oracle.  The sampled heads are regenerated on their own, so
+    host memory holds the prompt/decode layout once."""
+    from adaptive_head_kv_gb300.session import FastGenSession, make_params
+    from synth import make_workload, make_workload_split, punct_ids, special_ids
+
+    cfg = CONFIGS["llama65b"]
+    n, steps, dev = cfg.n, cfg.steps, torch.device("cuda")
+    w = make_workload_split(cfg)
+    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    s = FastGenSession(p, special_ids(), punct_ids(), steps)
+    ids = torch.from_numpy(w["ids"]).to(dev)
+    Q, K, V = (w.pop(x).to(dev) for x in "QKV")
+    s.prefill(Q, K, V, ids[:, :n].contiguous())
+    del Q, K, V
+    q, k, v = (w.pop(x).to(dev) for x in "qkv")
+    graph, outs = s.capture_decode(q, k, v, ids[:, n:].transpose(0, 1).contiguous(), n)
+    graph.replay()
+    torch.cuda.synchronize()
+    del q, k, v
+    gpu = dict(policy=s.policy.cpu().numpy().astype(int),
+               mass=s.mass.cpu().numpy().astype(np.float64), cost=s.cost.cpu().numpy(),
+               colsum=s.colsum.cpu().numpy().astype(np.float64), keep=s.keep.cpu().numpy(),
+               kept=s.kept.cpu().numpy(), out=_HeadColumns(outs), desc1=s.descriptors(),
+               pos1=s.pos_pool.cpu().numpy())
+    assert int(s.dev_err.item()) == 0
+    heads = sample_heads(cfg, w["types"], 16)
+    gpu["workload"] = make_workload(cfg, heads=heads)
+    rep = compare(cfg, gpu, range(len(heads)))
+    assert rep["decode_checked"] >= 10, rep
