@@ -15,8 +15,9 @@
 //   * writes (max, sum, acc[d]) per query for the item.
 // A second launch merges each query head's items (log-sum-exp merge), writes
 // out[g] and bumps the cache's never-evicted row count.  Both are launched as
-// programmatic dependents of the kernel before them.  HBM-bound: no tensor
-// cores (at most 8 queries share a K/V row).
+// programmatic dependents of the kernel before them.  With one query per
+// cache the pass is HBM-bound on the SIMT lanes; grouped bf16 caches score
+// and accumulate with warp-level MMAs (split_mma_kernel).
 #include <type_traits>
 
 #include "fg_common.cuh"
@@ -47,6 +48,62 @@ __device__ __forceinline__ Placement place(const fg_head_desc& hd, const DecodeA
   return pl;
 }
 
+// The rows of one work item and the step's bookkeeping on them.
+struct Item {
+  int c;         // cache
+  int r0, r1;    // rows [r0, r1) of the segment
+  int new_slot;  // row of the new token in the segment, or -1
+  int evict;     // ring row that left the window, or -1
+  bool ring;     // the item covers the window ring (else the never-evicted segment)
+  long long base;  // first pool row of the segment
+};
+
+// Reads work item wi, writes the new token's row if its slot falls in the item
+// (the only writer of that row) and marks an evicted ring row empty.
+template <typename T, int D>
+__device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi) {
+  constexpr int LPR = D / Vec16<T>::kElems;
+  const int2 it = a.work[wi];
+  Item m;
+  m.c = it.x;
+  int chunk = it.y;
+  const fg_head_desc hd = a.desc[m.c];
+  const Placement pl = place(hd, a, HLkv, m.c);
+  const int nsc = cdiv(hd.static_cap, kRowsPerWork);
+  m.ring = chunk >= nsc;
+  m.evict = -1;
+  if (!m.ring) {
+    m.r0 = chunk * kRowsPerWork;
+    m.r1 = min(m.r0 + kRowsPerWork, hd.n_static + (pl.st ? 1 : 0));
+    m.base = hd.off;
+    m.new_slot = pl.st ? hd.n_static : -1;
+    if (pl.overflow && chunk == 0 && threadIdx.x == 0) atomicOr(a.dev_err, 1);
+  } else {
+    chunk -= nsc;
+    m.r0 = chunk * kRowsPerWork;
+    m.r1 = min(m.r0 + kRowsPerWork, hd.w);
+    m.base = hd.win_off;
+    const int slot = a.pos % hd.w;
+    m.new_slot = pl.ring_put ? slot : -1;
+    m.evict = pl.ring_put ? -1 : slot;  // the row that left the window
+  }
+  if (m.new_slot >= m.r0 && m.new_slot < m.r1) {
+    T* Kp = (T*)a.Kp;
+    T* Vp = (T*)a.Vp;
+    const T* kn = (const T*)a.k_new + (size_t)m.c * D;
+    const T* vn = (const T*)a.v_new + (size_t)m.c * D;
+    constexpr int E = Vec16<T>::kElems;
+    for (int v = threadIdx.x; v < LPR; v += blockDim.x) {
+      const size_t d = (size_t)(m.base + m.new_slot) * D + v * E;
+      *reinterpret_cast<uint4*>(Kp + d) = *reinterpret_cast<const uint4*>(kn + v * E);
+      *reinterpret_cast<uint4*>(Vp + d) = *reinterpret_cast<const uint4*>(vn + v * E);
+    }
+    if (threadIdx.x == 0) a.posp[m.base + m.new_slot] = a.pos;
+  }
+  if (m.evict >= m.r0 && m.evict < m.r1 && threadIdx.x == 0) a.posp[m.base + m.evict] = -1;
+  return m;
+}
+
 // R = queries per cache (group size).  Rows are unrolled by U per warp so
 // that 2 * U 16-byte loads per thread are in flight.
 template <typename T, int D, int R>
@@ -65,43 +122,14 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
   griddep_wait();
   griddep_launch_dependents();
   const int wi = blockIdx.x;
-  const int2 it = a.work[wi];
-  const int c = it.x;  // cache
-  int chunk = it.y;
-  const fg_head_desc hd = a.desc[c];
-  const Placement pl = place(hd, a, HLkv, c);
-  const int nsc = cdiv(hd.static_cap, kRowsPerWork);
-  const bool ring = chunk >= nsc;
-  int r0, r1, new_slot, evict = -1;
-  long long base;
-  if (!ring) {
-    r0 = chunk * kRowsPerWork;
-    r1 = min(r0 + kRowsPerWork, hd.n_static + (pl.st ? 1 : 0));
-    base = hd.off;
-    new_slot = pl.st ? hd.n_static : -1;
-    if (pl.overflow && chunk == 0 && threadIdx.x == 0) atomicOr(a.dev_err, 1);
-  } else {
-    chunk -= nsc;
-    r0 = chunk * kRowsPerWork;
-    r1 = min(r0 + kRowsPerWork, hd.w);
-    base = hd.win_off;
-    const int slot = a.pos % hd.w;
-    new_slot = pl.ring_put ? slot : -1;
-    evict = pl.ring_put ? -1 : slot;  // the row that left the window
-  }
-  T* Kp = (T*)a.Kp;
-  T* Vp = (T*)a.Vp;
+  const Item it = item_setup<T, D>(a, HLkv, wi);
+  const int c = it.c, r0 = it.r0, r1 = it.r1, new_slot = it.new_slot, evict = it.evict;
+  const bool ring = it.ring;
+  const long long base = it.base;
+  const T* Kp = (const T*)a.Kp;
+  const T* Vp = (const T*)a.Vp;
   const T* kn = (const T*)a.k_new + (size_t)c * D;
   const T* vn = (const T*)a.v_new + (size_t)c * D;
-  if (new_slot >= r0 && new_slot < r1) {
-    for (int v = threadIdx.x; v < LPR; v += blockDim.x) {
-      const size_t d = (size_t)(base + new_slot) * D + v * E;
-      *reinterpret_cast<uint4*>(Kp + d) = *reinterpret_cast<const uint4*>(kn + v * E);
-      *reinterpret_cast<uint4*>(Vp + d) = *reinterpret_cast<const uint4*>(vn + v * E);
-    }
-    if (threadIdx.x == 0) a.posp[base + new_slot] = a.pos;
-  }
-  if (evict >= r0 && evict < r1 && threadIdx.x == 0) a.posp[base + evict] = -1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, gl = lane % LPR;
@@ -254,6 +282,240 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Grouped caches (R = 2, 4, 8 query heads per key/value head), bf16.
+//
+// Scoring every row against R queries on the SIMT lanes costs R dot products,
+// R lane reductions and R rescaled accumulators per row: at R >= 4 that is
+// instruction-bound well below the bandwidth of the row stream.  Here each
+// warp takes 16-row blocks and does both products as register-level bf16
+// MMAs (m16n8k16, fp32 accumulate), with the queries on the N = 8 side:
+//   S^T[16 keys x 8 q]  = K[16 keys x d] . Q^T[d x 8 q]
+//   O^T[d x 8 q]       += V^T[d x 16 keys] . P^T[16 keys x 8 q]
+// Operands come straight from HBM into registers: the d index of the score
+// contraction and the d index of O^T are permuted (the same permutation on
+// both operands, undone when O^T is stored) so that every lane's fragments
+// are whole 16-byte loads and every load instruction covers whole sectors.
+// P is split into a bf16 high part and a bf16 remainder (two MMAs), so the
+// weights carry ~16 significant bits, as the fp32 path does.  S^T's
+// accumulator fragment becomes P^T's operand fragment with one 8x8
+// transpose per half (movmatrix).  The tensor-core tile minimum of tcgen05
+// (M >= 64) is far above the 8 queries of a group, so these are warp MMAs.
+constexpr int kMmaWarps = 8;
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kMmaBlk = 16;                                   // rows per MMA tile
+constexpr int kMmaNB = kRowsPerWork / (kMmaWarps * kMmaBlk);  // blocks per warp
+static_assert(kMmaNB * kMmaWarps * kMmaBlk == kRowsPerWork, "item = whole blocks");
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one row pair per lane (lane l: row l/4,
+// columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// (lo, hi) -> bf16x2 with lo in the low half, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <int D, int R>
+__global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeArgs a, int H,
+                                                                int HLkv, float sl2) {
+  using T = __nv_bfloat16;
+  constexpr int KI = D / 32;  // 16-byte pieces of a K row per lane (2 k-steps each)
+  constexpr int VH = D / 64;  // 16-byte pieces of a V row per lane
+  constexpr int MT = D / 16;  // 16-row tiles of O^T
+  constexpr int NB = kMmaNB;
+  __shared__ float sm_m[kMmaWarps][R], sm_l[kMmaWarps][R];
+  __shared__ float sm_f[kMmaWarps][R];
+  __shared__ __align__(16) float sm_acc[kMmaWarps][R][D];
+
+  griddep_wait();
+  griddep_launch_dependents();
+  const int wi = blockIdx.x;
+  const Item it = item_setup<T, D>(a, HLkv, wi);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const T* Kp = (const T*)a.Kp;
+  const T* Vp = (const T*)a.Vp;
+  const T* kn = (const T*)a.k_new + (size_t)it.c * D;
+  const T* vn = (const T*)a.v_new + (size_t)it.c * D;
+  const int Hkv = H / R;
+  const size_t g0 = (size_t)(it.c / Hkv) * H + (size_t)(it.c % Hkv) * R;  // first query head
+
+  auto row_ok = [&](int r) -> bool {
+    if (r >= it.r1) return false;
+    if (r == it.new_slot || !it.ring) return true;
+    return r != it.evict && a.posp[it.base + r] >= 0;
+  };
+  auto krow = [&](int r) { return r == it.new_slot ? kn : Kp + (size_t)(it.base + r) * D; };
+  auto vrow = [&](int r) { return r == it.new_slot ? vn : Vp + (size_t)(it.base + r) * D; };
+
+  // Q^T operand: lane (g, t4) holds query g's elements {32 i + 8 t4 .. + 7}
+  // (zero for g >= R); k-step 2i + h takes words 2h, 2h + 1 of piece i.
+  uint4 qv[KI];
+  {
+    const T* qr = (const T*)a.q + (g0 + (g < R ? g : 0)) * D;
+#pragma unroll
+    for (int i = 0; i < KI; ++i)
+      qv[i] = g < R ? *reinterpret_cast<const uint4*>(qr + 32 * i + 8 * t4) : make_uint4(0, 0, 0, 0);
+  }
+
+  // Per warp: blocks warp and warp + 8 of the item, one after the other, with
+  // an online softmax across them (kept to one block of loads in flight per
+  // warp, so that two CTAs fit on an SM and overlap each other's phases).
+  float m[2] = {FG_NEG_INF, FG_NEG_INF}, l[2] = {0.f, 0.f};
+  float o[MT][4];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll 1
+  for (int b = 0; b < NB; ++b) {
+    const int rb = it.r0 + (warp + kMmaWarps * b) * kMmaBlk;
+    if (rb >= it.r1) break;
+    // K: rows g and g + 8 of the block, pieces {32 i + 8 t4}.
+    // V: rows 2t4, 2t4+1, 2t4+8, 2t4+9, pieces {64 h + 8 g}.
+    uint4 kr[2][KI], vr[4][VH];
+    bool kok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rb + g + 8 * h;
+      kok[h] = row_ok(r);
+      const T* p = krow(r);
+#pragma unroll
+      for (int i = 0; i < KI; ++i)
+        kr[h][i] = kok[h] ? ldg_stream(p + 32 * i + 8 * t4) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = rb + 2 * t4 + (j & 1) + 8 * (j >> 1);
+      const bool ok = row_ok(r);  // empty ring slots may hold anything: never read them
+      const T* p = vrow(r);
+#pragma unroll
+      for (int h = 0; h < VH; ++h)
+        vr[j][h] = ok ? ldg_stream(p + 64 * h + 8 * g) : make_uint4(0, 0, 0, 0);
+    }
+    // scores, base-2 units: (key g, q 2t4), (key g, q 2t4+1), (key g+8, q 2t4),
+    // (key g+8, q 2t4+1)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < KI; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        mma_bf16_16816(sc, word(kr[0][i], 2 * h), word(kr[1][i], 2 * h),
+                       word(kr[0][i], 2 * h + 1), word(kr[1][i], 2 * h + 1), word(qv[i], 2 * h),
+                       word(qv[i], 2 * h + 1));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[e] = kok[e >> 1] ? sc[e] * sl2 : FG_NEG_INF;
+    // per query column: max over the block's rows (lanes of equal t4), then
+    // the running max and the rescale of what is accumulated
+    float me[2];
+#pragma unroll
+    for (int qc = 0; qc < 2; ++qc) {
+      float v = fmaxf(sc[qc], sc[qc + 2]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+      const float mn = fmaxf(m[qc], v);
+      const float corr = mn == FG_NEG_INF ? 1.f : exp2f(m[qc] - mn);
+      l[qc] *= corr;
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        o[j][qc] *= corr;
+        o[j][qc + 2] *= corr;
+      }
+      m[qc] = mn;
+      me[qc] = mn == FG_NEG_INF ? 0.f : mn;
+    }
+    float p[4];
+    p[0] = exp2f(sc[0] - me[0]);
+    p[1] = exp2f(sc[1] - me[1]);
+    p[2] = exp2f(sc[2] - me[0]);
+    p[3] = exp2f(sc[3] - me[1]);
+    l[0] += p[0] + p[2];
+    l[1] += p[1] + p[3];
+    const uint32_t hi0 = pack_bf16x2(p[0], p[1]), hi1 = pack_bf16x2(p[2], p[3]);
+    const uint32_t lo0 = pack_bf16x2(p[0] - bf16_lo(hi0), p[1] - bf16_hi(hi0));
+    const uint32_t lo1 = pack_bf16x2(p[2] - bf16_lo(hi1), p[3] - bf16_hi(hi1));
+    const uint32_t bh0 = transpose8x8(hi0), bh1 = transpose8x8(hi1);
+    const uint32_t bl0 = transpose8x8(lo0), bl1 = transpose8x8(lo1);
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      const int h = j >> 2, w = j & 3;
+      const uint32_t x0 = word(vr[0][h], w), x1 = word(vr[1][h], w);
+      const uint32_t x2 = word(vr[2][h], w), x3 = word(vr[3][h], w);
+      const uint32_t a0 = __byte_perm(x0, x1, 0x5410), a1 = __byte_perm(x0, x1, 0x7632);
+      const uint32_t a2 = __byte_perm(x2, x3, 0x5410), a3 = __byte_perm(x2, x3, 0x7632);
+      mma_bf16_16816(o[j], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16_16816(o[j], a0, a1, a2, a3, bl0, bl1);
+    }
+  }
+#pragma unroll
+  for (int qc = 0; qc < 2; ++qc)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l[qc] += __shfl_xor_sync(0xffffffffu, l[qc], off);
+  const float mx[2] = {m[0], m[1]};
+
+  // O^T fragment of tile j: rows d = 64 (j/4) + 8 g + 2 (j%4) and d + 1,
+  // columns q = 2t4, 2t4 + 1.
+#pragma unroll
+  for (int qc = 0; qc < 2; ++qc) {
+    const int q = 2 * t4 + qc;
+    if (q < R) {
+      if (g == 0) {
+        sm_m[warp][q] = mx[qc];
+        sm_l[warp][q] = l[qc];
+      }
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        const int d = 64 * (j >> 2) + 8 * g + 2 * (j & 3);
+        *reinterpret_cast<float2*>(&sm_acc[warp][q][d]) = make_float2(o[j][qc], o[j][qc + 2]);
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < R) {
+    const int q = threadIdx.x;
+    float M = FG_NEG_INF;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, sm_m[w][q]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) {
+      const float f = M == FG_NEG_INF || sm_m[w][q] == FG_NEG_INF ? 0.f : exp2f(sm_m[w][q] - M);
+      sm_f[w][q] = f;
+      L += sm_l[w][q] * f;
+    }
+    const size_t slot = (size_t)wi * R + q;
+    a.part_ml[2 * slot] = M;
+    a.part_ml[2 * slot + 1] = L;
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < R * D; x += kMmaThreads) {
+    const int q = x / D, d = x % D;
+    float A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) A = fmaf(sm_f[w][q], sm_acc[w][q][d], A);
+    a.part_acc[((size_t)wi * R + q) * D + d] = A;
+  }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G, int H, int R,
                                                       int HLkv) {
@@ -309,8 +571,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G,
 
 template <typename T, int D, int R>
 cudaError_t run(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(split_kernel<T, D, R>, a.n_work, kDecThreads, 0, s, a, pd.H, pd.HLkv,
-                             pd.sl2);
+  cudaError_t e;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && R >= 2)
+    e = launch_pdl(split_mma_kernel<D, R>, a.n_work, kMmaThreads, 0, s, a, pd.H, pd.HLkv, pd.sl2);
+  else
+    e = launch_pdl(split_kernel<T, D, R>, a.n_work, kDecThreads, 0, s, a, pd.H, pd.HLkv, pd.sl2);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, 0, s, a, pd.G, pd.H, pd.R, pd.HLkv);
   return e;
