@@ -516,54 +516,36 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
   }
 }
 
+// One CTA of D threads per query head, thread t = dimension t: every thread
+// forms the item weights itself (a few exp2 per item, from broadcast loads)
+// and sums its dimension over the items, so each item costs one coalesced
+// row load for the whole CTA.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int G, int H, int R,
-                                                      int HLkv) {
-  constexpr int PL = D / 32;
+__global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, int R, int HLkv) {
   griddep_wait();
   griddep_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x * 8 + warp;  // query head
-  if (g >= G) return;
+  const int g = blockIdx.x;  // query head
+  const int t = threadIdx.x;
   const int c = kv_head(g, H, R), q = (g % H) % R;  // its cache and place in the group
   const fg_head_desc hd = a.desc[c];
   const size_t w0 = (size_t)hd.work_off;
-  // items in groups of 32: lane i holds item i's (max, sum); the weights are
-  // then broadcast while every lane sums its PL dimensions over the items
+  const int nw = hd.n_work;
   float M = FG_NEG_INF;
-  for (int i = lane; i < hd.n_work; i += 32) M = fmaxf(M, a.part_ml[2 * ((w0 + i) * R + q)]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float L = 0.f, acc[PL];
-#pragma unroll
-  for (int e = 0; e < PL; ++e) acc[e] = 0.f;
-  if (M != FG_NEG_INF) {
-    for (int base = 0; base < hd.n_work; base += 32) {
-      const int i = base + lane;
-      float wgt = 0.f;
-      if (i < hd.n_work) {
-        const size_t slot = (w0 + i) * R + q;
-        const float mi = a.part_ml[2 * slot];
-        wgt = mi == FG_NEG_INF ? 0.f : exp2f(mi - M);
-        L += wgt * a.part_ml[2 * slot + 1];
-      }
-      const int cnt = min(32, hd.n_work - base);
 #pragma unroll 4
-      for (int j = 0; j < cnt; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, wgt, j);
-        const float* pa = a.part_acc + ((w0 + base + j) * R + q) * D + lane * PL;
-#pragma unroll
-        for (int e = 0; e < PL; ++e) acc[e] = fmaf(wj, pa[e], acc[e]);
-      }
+  for (int i = 0; i < nw; ++i) M = fmaxf(M, a.part_ml[2 * ((w0 + i) * R + q)]);
+  float L = 0.f, acc = 0.f;
+  if (M != FG_NEG_INF) {
+#pragma unroll 4
+    for (int i = 0; i < nw; ++i) {
+      const size_t slot = (w0 + i) * R + q;
+      const float mi = a.part_ml[2 * slot];
+      const float wgt = mi == FG_NEG_INF ? 0.f : exp2f(mi - M);
+      L = fmaf(wgt, a.part_ml[2 * slot + 1], L);
+      acc = fmaf(wgt, a.part_acc[slot * D + t], acc);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   }
-  T* out = (T*)a.out + (size_t)g * D;
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-  for (int e = 0; e < PL; ++e) store_out(out + lane * PL + e, acc[e] * inv);
-  if (lane == 0 && q == 0) {  // one member advances the shared cache
+  store_out((T*)a.out + (size_t)g * D + t, L > 0.f ? acc / L : 0.f);
+  if (t == 0 && q == 0) {  // one member advances the shared cache
     const Placement pl = place(hd, a, HLkv, c);
     if (pl.st) a.desc[c].n_static = hd.n_static + 1;
   }
@@ -577,7 +559,7 @@ cudaError_t run(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
   else
     e = launch_pdl(split_kernel<T, D, R>, a.n_work, kDecThreads, 0, s, a, pd.H, pd.HLkv, pd.sl2);
   if (e == cudaSuccess)
-    e = launch_pdl(combine_kernel<T, D>, cdiv(pd.G, 8), 256, 0, s, a, pd.G, pd.H, pd.R, pd.HLkv);
+    e = launch_pdl(combine_kernel<T, D>, pd.G, D, 0, s, a, pd.H, pd.R, pd.HLkv);
   return e;
 }
 
