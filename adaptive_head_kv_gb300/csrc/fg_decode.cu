@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 }
 
 // ---------------------------------------------------------------------------
-// Grouped caches (R = 2, 4, 8 query heads per key/value head), bf16.
+// bf16 caches on warp MMAs.
 //
 // Scoring every row against R queries on the SIMT lanes costs R dot products,
 // R lane reductions and R rescaled accumulators per row: at R >= 4 that is
@@ -292,20 +292,35 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 // MMAs (m16n8k16, fp32 accumulate), with the queries on the N = 8 side:
 //   S^T[16 keys x 8 q]  = K[16 keys x d] . Q^T[d x 8 q]
 //   O^T[d x 8 q]       += V^T[d x 16 keys] . P^T[16 keys x 8 q]
-// Operands come straight from HBM into registers: the d index of the score
-// contraction and the d index of O^T are permuted (the same permutation on
-// both operands, undone when O^T is stored) so that every lane's fragments
-// are whole 16-byte loads and every load instruction covers whole sectors.
-// P is split into a bf16 high part and a bf16 remainder (two MMAs), so the
-// weights carry ~16 significant bits, as the fp32 path does.  S^T's
-// accumulator fragment becomes P^T's operand fragment with one 8x8
-// transpose per half (movmatrix).  The tensor-core tile minimum of tcgen05
-// (M >= 64) is far above the 8 queries of a group, so these are warp MMAs.
-constexpr int kMmaWarps = 8;
+// Rows reach shared memory through cp.async (16-byte pieces, zero-filled for
+// rows that must not be read, the new token's row taken from the step's
+// input), in a per-warp ring of kMmaStages blocks, so loads stay in flight
+// without holding registers; fragments come from ldmatrix (K) and
+// ldmatrix.trans (V) on rows padded by 16 bytes (conflict-free).  P is split
+// into a bf16 high part and a bf16 remainder (two MMAs), so the weights keep
+// ~16 significant bits, as the fp32 SIMT path does.  S^T's accumulator
+// fragment becomes P^T's operand fragment with one 8x8 transpose per half
+// (movmatrix).  tcgen05's smallest tile (M >= 64) is far above the <= 8
+// queries of a group, so these are warp MMAs.
+constexpr int kMmaWarps = 4;
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaBlk = 16;                                   // rows per MMA tile
 constexpr int kMmaNB = kRowsPerWork / (kMmaWarps * kMmaBlk);  // blocks per warp
+constexpr int kMmaStages = 2;                                 // V blocks in flight per warp
 static_assert(kMmaNB * kMmaWarps * kMmaBlk == kRowsPerWork, "item = whole blocks");
+
+template <int D>
+struct MmaSmem {
+  static constexpr int kStride = D + 8;                        // padded V row, elements
+  static constexpr int kStageElems = kMmaBlk * kStride;
+  static constexpr size_t kRingBytes = (size_t)kMmaWarps * kMmaStages * kStageElems * 2;
+  template <int R>
+  static constexpr size_t bytes() {
+    // the merge buffers reuse the rings once every warp is done with them
+    constexpr size_t merge = (size_t)kMmaWarps * R * D * 4;
+    return kRingBytes > merge ? kRingBytes : merge;
+  }
+};
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
@@ -332,21 +347,53 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte global -> shared copy; bytes past src_bytes (0 or 16) are zeroed.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 template <int D, int R>
-__global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeArgs a, int H,
-                                                                int HLkv, float sl2) {
+__global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeArgs a, int H,
+                                                                   int HLkv, float sl2) {
   using T = __nv_bfloat16;
-  constexpr int KI = D / 32;  // 16-byte pieces of a K row per lane (2 k-steps each)
-  constexpr int VH = D / 64;  // 16-byte pieces of a V row per lane
-  constexpr int MT = D / 16;  // 16-row tiles of O^T
-  constexpr int NB = kMmaNB;
-  __shared__ float sm_m[kMmaWarps][R], sm_l[kMmaWarps][R];
-  __shared__ float sm_f[kMmaWarps][R];
-  __shared__ __align__(16) float sm_acc[kMmaWarps][R][D];
+  using SM = MmaSmem<D>;
+  constexpr int KI = D / 32;       // 16-byte pieces of a K row per lane (2 k-steps each)
+  constexpr int MT = D / 16;       // 16-row tiles of O^T
+  constexpr int PPR = D / 8;       // 16-byte pieces per V row
+  constexpr int NP = kMmaBlk * PPR / 32;  // V pieces per lane per block
+  constexpr int STR = SM::kStride;
+  extern __shared__ __align__(16) uint8_t mma_smem[];
+  __shared__ float sm_m[kMmaWarps][R], sm_l[kMmaWarps][R], sm_f[kMmaWarps][R];
 
   griddep_wait();
   griddep_launch_dependents();
@@ -366,11 +413,43 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
     if (r == it.new_slot || !it.ring) return true;
     return r != it.evict && a.posp[it.base + r] >= 0;
   };
-  auto krow = [&](int r) { return r == it.new_slot ? kn : Kp + (size_t)(it.base + r) * D; };
-  auto vrow = [&](int r) { return r == it.new_slot ? vn : Vp + (size_t)(it.base + r) * D; };
+  // This warp's blocks: rows first + W*16*b, b = 0 .. nblk-1, one after the
+  // other with an online softmax across them.  K rows go to registers: the
+  // next block's are requested as soon as the scores are formed.  V rows go
+  // through a two-stage shared-memory ring by cp.async, the next block's
+  // requested before this block's scores.
+  const int first = it.r0 + warp * kMmaBlk;
+  const int nblk =
+      first < it.r1 ? min(kMmaNB, cdiv(it.r1 - first, kMmaWarps * kMmaBlk)) : 0;
+  const uint32_t vring =
+      smem_u32(mma_smem) + (uint32_t)(warp * kMmaStages * SM::kStageElems * 2);
+  // K: rows g and g + 8 of a block, pieces {32 i + 8 t4}; k-step 2i + h takes
+  // words 2h (d positions 2t4, 2t4+1) and 2h + 1 (positions 2t4+8, 2t4+9) of
+  // piece i.  Q^T is loaded with the same permutation of d.
+  auto load_k = [&](int rb, uint4 (&kr)[2][KI], bool (&kok)[2]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rb + g + 8 * h;
+      kok[h] = row_ok(r);
+      const T* p = r == it.new_slot ? kn : Kp + (size_t)(it.base + r) * D;
+#pragma unroll
+      for (int i = 0; i < KI; ++i)
+        kr[h][i] = kok[h] ? ldg_stream(p + 32 * i + 8 * t4) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto issue_v = [&](int rb, int st) {
+    const uint32_t vs = vring + (uint32_t)(st * SM::kStageElems * 2);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int pc = (lane + 32 * i) % PPR, row = (lane + 32 * i) / PPR;
+      const int r = rb + row;
+      const bool ok = row_ok(r);  // empty ring slots may hold anything: never read them
+      const T* src = !ok ? vn : r == it.new_slot ? vn + pc * 8
+                                                  : Vp + (size_t)(it.base + r) * D + pc * 8;
+      cp_async16(vs + (uint32_t)((row * STR + pc * 8) * 2), src, ok ? 16 : 0);
+    }
+  };
 
-  // Q^T operand: lane (g, t4) holds query g's elements {32 i + 8 t4 .. + 7}
-  // (zero for g >= R); k-step 2i + h takes words 2h, 2h + 1 of piece i.
   uint4 qv[KI];
   {
     const T* qr = (const T*)a.q + (g0 + (g < R ? g : 0)) * D;
@@ -378,40 +457,27 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
     for (int i = 0; i < KI; ++i)
       qv[i] = g < R ? *reinterpret_cast<const uint4*>(qr + 32 * i + 8 * t4) : make_uint4(0, 0, 0, 0);
   }
-
-  // Per warp: blocks warp and warp + 8 of the item, one after the other, with
-  // an online softmax across them (kept to one block of loads in flight per
-  // warp, so that two CTAs fit on an SM and overlap each other's phases).
   float m[2] = {FG_NEG_INF, FG_NEG_INF}, l[2] = {0.f, 0.f};
   float o[MT][4];
 #pragma unroll
   for (int j = 0; j < MT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  uint4 kr[2][KI];
+  bool kok[2];
+  if (nblk > 0) {
+    load_k(first, kr, kok);
+    issue_v(first, 0);
+  }
+  cp_async_commit();
+  // ldmatrix row addresses: lane l serves matrix l/8, row l%8; V^T tile j:
+  // matrices (keys 8(lm>>1).., d 16j + 8(lm&1)..), transposed
+  const int lm = lane >> 3, lr = lane & 7;
+  const uint32_t vlane = (uint32_t)(((lr + 8 * (lm >> 1)) * STR + 8 * (lm & 1)) * 2);
 #pragma unroll 1
-  for (int b = 0; b < NB; ++b) {
-    const int rb = it.r0 + (warp + kMmaWarps * b) * kMmaBlk;
-    if (rb >= it.r1) break;
-    // K: rows g and g + 8 of the block, pieces {32 i + 8 t4}.
-    // V: rows 2t4, 2t4+1, 2t4+8, 2t4+9, pieces {64 h + 8 g}.
-    uint4 kr[2][KI], vr[4][VH];
-    bool kok[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = rb + g + 8 * h;
-      kok[h] = row_ok(r);
-      const T* p = krow(r);
-#pragma unroll
-      for (int i = 0; i < KI; ++i)
-        kr[h][i] = kok[h] ? ldg_stream(p + 32 * i + 8 * t4) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = rb + 2 * t4 + (j & 1) + 8 * (j >> 1);
-      const bool ok = row_ok(r);  // empty ring slots may hold anything: never read them
-      const T* p = vrow(r);
-#pragma unroll
-      for (int h = 0; h < VH; ++h)
-        vr[j][h] = ok ? ldg_stream(p + 64 * h + 8 * g) : make_uint4(0, 0, 0, 0);
-    }
+  for (int b = 0; b < nblk; ++b) {
+    const int rb = first + b * kMmaWarps * kMmaBlk, rn = rb + kMmaWarps * kMmaBlk;
+    const bool more = b + 1 < nblk;
+    if (more) issue_v(rn, (b + 1) % kMmaStages);
+    cp_async_commit();
     // scores, base-2 units: (key g, q 2t4), (key g, q 2t4+1), (key g+8, q 2t4),
     // (key g+8, q 2t4+1)
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -424,6 +490,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
                        word(qv[i], 2 * h + 1));
 #pragma unroll
     for (int e = 0; e < 4; ++e) sc[e] = kok[e >> 1] ? sc[e] * sl2 : FG_NEG_INF;
+    if (more) load_k(rn, kr, kok);  // the K registers are free now
     // per query column: max over the block's rows (lanes of equal t4), then
     // the running max and the rescale of what is accumulated
     float me[2];
@@ -455,37 +522,41 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
     const uint32_t lo1 = pack_bf16x2(p[2] - bf16_lo(hi1), p[3] - bf16_hi(hi1));
     const uint32_t bh0 = transpose8x8(hi0), bh1 = transpose8x8(hi1);
     const uint32_t bl0 = transpose8x8(lo0), bl1 = transpose8x8(lo1);
+    cp_async_wait<1>();  // this block's V rows have landed
+    __syncwarp();
+    {
+      const uint32_t vaddr = vring + (uint32_t)((b % kMmaStages) * SM::kStageElems * 2) + vlane;
 #pragma unroll
-    for (int j = 0; j < MT; ++j) {
-      const int h = j >> 2, w = j & 3;
-      const uint32_t x0 = word(vr[0][h], w), x1 = word(vr[1][h], w);
-      const uint32_t x2 = word(vr[2][h], w), x3 = word(vr[3][h], w);
-      const uint32_t a0 = __byte_perm(x0, x1, 0x5410), a1 = __byte_perm(x0, x1, 0x7632);
-      const uint32_t a2 = __byte_perm(x2, x3, 0x5410), a3 = __byte_perm(x2, x3, 0x7632);
-      mma_bf16_16816(o[j], a0, a1, a2, a3, bh0, bh1);
-      mma_bf16_16816(o[j], a0, a1, a2, a3, bl0, bl1);
+      for (int j = 0; j < MT; ++j) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vaddr + j * 32, a0, a1, a2, a3);
+        mma_bf16_16816(o[j], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(o[j], a0, a1, a2, a3, bl0, bl1);
+      }
     }
+    __syncwarp();  // the stage is refilled two blocks later
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int qc = 0; qc < 2; ++qc)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l[qc] += __shfl_xor_sync(0xffffffffu, l[qc], off);
-  const float mx[2] = {m[0], m[1]};
 
-  // O^T fragment of tile j: rows d = 64 (j/4) + 8 g + 2 (j%4) and d + 1,
-  // columns q = 2t4, 2t4 + 1.
+  // O^T fragment of tile j: rows d = 16 j + g and d + 8, columns q = 2t4, 2t4 + 1.
+  __syncthreads();  // every warp is done with its ring: the merge buffers reuse it
+  float* sm_acc = reinterpret_cast<float*>(mma_smem);  // [W][R][D]
 #pragma unroll
   for (int qc = 0; qc < 2; ++qc) {
     const int q = 2 * t4 + qc;
     if (q < R) {
       if (g == 0) {
-        sm_m[warp][q] = mx[qc];
+        sm_m[warp][q] = m[qc];
         sm_l[warp][q] = l[qc];
       }
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
-        const int d = 64 * (j >> 2) + 8 * g + 2 * (j & 3);
-        *reinterpret_cast<float2*>(&sm_acc[warp][q][d]) = make_float2(o[j][qc], o[j][qc + 2]);
+        sm_acc[(warp * R + q) * D + 16 * j + g] = o[j][qc];
+        sm_acc[(warp * R + q) * D + 16 * j + g + 8] = o[j][qc + 2];
       }
     }
   }
@@ -511,7 +582,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_mma_kernel(const DecodeA
     const int q = x / D, d = x % D;
     float A = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w) A = fmaf(sm_f[w][q], sm_acc[w][q][d], A);
+    for (int w = 0; w < kMmaWarps; ++w) A = fmaf(sm_f[w][q], sm_acc[(w * R + q) * D + d], A);
     a.part_acc[((size_t)wi * R + q) * D + d] = A;
   }
 }
@@ -554,10 +625,16 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
 template <typename T, int D, int R>
 cudaError_t run(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e;
-  if constexpr (std::is_same<T, __nv_bfloat16>::value && R >= 2)
-    e = launch_pdl(split_mma_kernel<D, R>, a.n_work, kMmaThreads, 0, s, a, pd.H, pd.HLkv, pd.sl2);
-  else
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && R >= 2) {
+    constexpr size_t smem = MmaSmem<D>::template bytes<R>();
+    e = cudaFuncSetAttribute(split_mma_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e == cudaSuccess)
+      e = launch_pdl(split_mma_kernel<D, R>, a.n_work, kMmaThreads, smem, s, a, pd.H, pd.HLkv,
+                     pd.sl2);
+  } else {
     e = launch_pdl(split_kernel<T, D, R>, a.n_work, kDecThreads, 0, s, a, pd.H, pd.HLkv, pd.sl2);
+  }
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel<T, D>, pd.G, D, 0, s, a, pd.H, pd.R, pd.HLkv);
   return e;
