@@ -44,6 +44,13 @@ Readings of points the pages leave open (each is listed in the design notes):
      leave the cache; window members leave it once they are w positions old.
      The frequent set is frozen at the prompt.  The query attends over the
      cache after the new token is placed; an empty cache yields zeros.
+  R11 a saved head-policy map (the overview page's offline head-type map,
+     read together with the Method's policy reuse) fixes each head's
+     shortlist entry for a later prompt; that prompt's caches are the
+     entry's final sets built from the prompt itself (its special and
+     punctuation ids, its last w positions, the top-k of its own cumulative
+     attention scores).  Only entries containing C_frequent need the scores;
+     no masses are formed and no choice is made.
 """
 from __future__ import annotations
 
@@ -312,3 +319,41 @@ def decode_group(policy, keep, n, w, ids, Qalls, Kall, Vall, special_ids, punct_
         for m, Qall in enumerate(Qalls):
             out[m, step] = attend(np.asarray(Qall, dtype=np.float64)[t], Kall[pos], Vall[pos], s)
     return out, pos
+
+
+# --- policy reuse with a saved head-policy map (R11) ----------------------
+
+def keep_for_policy(policy, ids, special_ids, punct_ids, r_l, r_f, n, colsum=None):
+    """Keep codes of shortlist entry `policy` on a prompt of n tokens (R11).
+
+    The cache is the entry's final set (final_sets): special / punctuation
+    positions from the prompt's ids, the last w = ceil(r_l n) positions for
+    the local part, and the top k = ceil(r_f n) keys of the prompt's own
+    cumulative attention scores `colsum` for the frequent part.  `colsum` is
+    required exactly when the entry contains C_frequent.
+    """
+    n = int(n)
+    spec, punc = token_sets(np.asarray(ids)[:n], special_ids, punct_ids)
+    w, k = ratio_count(r_l, n), ratio_count(r_f, n)
+    if policy in (P_SPF, P_SPFL):
+        if colsum is None:
+            raise ValueError("entries containing C_frequent need the column sums")
+        freq = frequent_set(np.asarray(colsum, dtype=np.float64), k)
+    else:
+        freq = np.zeros(n, dtype=bool)
+    return final_sets(n, spec, punc, freq, w)[policy]
+
+
+def profile_with_policy(policy, Q, K, ids, special_ids, punct_ids, r_l, r_f, scale=None):
+    """One head of a later prompt under a saved policy (R11): the attention
+    map and its column sums are formed only when the entry needs C_frequent.
+    Returns dict(keep, kept, colsum or None)."""
+    Q = np.asarray(Q, dtype=np.float64)
+    n, d = Q.shape
+    colsum = None
+    if policy in (P_SPF, P_SPFL):
+        s = default_scale(d) if scale is None else scale
+        colsum = cumulative_scores(attention_map(Q, np.asarray(K, dtype=np.float64), s))
+    keep = keep_for_policy(policy, ids, special_ids, punct_ids, r_l, r_f, n, colsum)
+    return dict(keep=keep, kept=int((keep != DROP).sum()), colsum=colsum)
+
