@@ -100,7 +100,58 @@ size_t fastgen_profile_workspace_bytes(const fg_params* p) {
   if (check_params(p) != FG_OK) return 0;
   const size_t G = (size_t)p->B * p->L * p->H, n = p->n;
   return align_up(G * fg::lse_ld(p->n) * sizeof(float)) + align_up(G * n * sizeof(float)) +
-         align_up((size_t)p->B * n) + kAlign;
+         align_up((size_t)p->B * n) + kAlign + align_up(G * sizeof(int32_t));
+}
+
+// Shared by fastgen_profile (fixed == NULL) and fastgen_profile_with_policy.
+static fg_status profile_call(const fg_params* p, const void* Q, const void* K,
+                              const int32_t* token_ids, const int32_t* special_ids,
+                              int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                              const int8_t* fixed, int8_t* policy, float* mass, int32_t* cost,
+                              float* colsum, uint8_t* keep, int32_t* kept, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
+  if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
+  if (!Q || !K || !token_ids || !colsum || !keep || !kept || !workspace || !dev_err)
+    return FG_EINVAL;
+  if (!fixed && (!policy || !mass || !cost)) return FG_EINVAL;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(workspace, kAlign) ||
+      !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4) ||
+      !aligned(dev_err, 4) || (!fixed && (!aligned(mass, 4) || !aligned(cost, 4))))
+    return FG_EINVAL;
+  if (workspace_bytes < fastgen_profile_workspace_bytes(p)) return FG_EWORKSPACE;
+  const fg::ProfileDims pd = dims(p);
+  const size_t Gn = (size_t)pd.G * pd.n;
+  const int ld = fg::lse_ld(pd.n);
+  // workspace: [lse2 G x ld][bandcol G x n][token classes B x n][256: counters][head list G]
+  char* ws = (char*)workspace;
+  float* lse2 = (float*)ws;
+  size_t off = align_up((size_t)pd.G * ld * sizeof(float));
+  float* bandcol = (float*)(ws + off);
+  off += align_up(Gn * sizeof(float));
+  uint8_t* cls = (uint8_t*)(ws + off);
+  off += align_up((size_t)pd.B * pd.n);
+  int32_t* sched = (int32_t*)(ws + off);  // [0], [1] zeroed by the class kernel; [2] head count
+  off += kAlign;
+  int32_t* heads = (int32_t*)(ws + off);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
+                                         punct_ids, n_punct, cls, sched, s);
+  const bool tc = fg::profile_tc_supported(pd);
+  if (e == cudaSuccess && fixed && tc) e = fg::launch_head_list(fixed, pd.G, heads, sched + 2, s);
+  if (e == cudaSuccess) {
+    if (tc)
+      e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, fixed ? heads : nullptr,
+                                fixed ? sched + 2 : nullptr, sched, dev_err, s);
+    else  // the fp32 path scores every head
+      e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
+  }
+  if (e == cudaSuccess)
+    e = fg::launch_select(pd, colsum, bandcol, cls, fixed, policy, mass, cost, keep, kept,
+                          dev_err, s);
+  return cuda_status(e);
 }
 
 fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
@@ -109,40 +160,21 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           int8_t* policy, float* mass, int32_t* cost, float* colsum,
                           uint8_t* keep, int32_t* kept, void* workspace,
                           size_t workspace_bytes, int32_t* dev_err, void* stream) {
-  fg_status st = check_params(p);
-  if (st != FG_OK) return st;
-  if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
-  if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
-  if (!Q || !K || !token_ids || !policy || !mass || !cost || !colsum || !keep || !kept ||
-      !workspace || !dev_err)
-    return FG_EINVAL;
-  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(workspace, kAlign) || !aligned(mass, 4) ||
-      !aligned(cost, 4) || !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4) ||
-      !aligned(dev_err, 4))
-    return FG_EINVAL;
-  if (workspace_bytes < fastgen_profile_workspace_bytes(p)) return FG_EWORKSPACE;
-  const fg::ProfileDims pd = dims(p);
-  const size_t Gn = (size_t)pd.G * pd.n;
-  const int ld = fg::lse_ld(pd.n);
-  char* ws = (char*)workspace;
-  float* lse2 = (float*)ws;
-  const size_t lse_bytes = align_up((size_t)pd.G * ld * sizeof(float));
-  float* bandcol = (float*)(ws + lse_bytes);
-  uint8_t* cls = (uint8_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)));
-  int32_t* sched = (int32_t*)(ws + lse_bytes + align_up(Gn * sizeof(float)) +
-                              align_up((size_t)pd.B * pd.n));  // zeroed by the class kernel
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = fg::launch_token_class(token_ids, pd.B * pd.n, special_ids, n_special,
-                                         punct_ids, n_punct, cls, sched, s);
-  if (e == cudaSuccess) {
-    if (fg::profile_tc_supported(pd))
-      e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, sched, dev_err, s);
-    else
-      e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
-  }
-  if (e == cudaSuccess)
-    e = fg::launch_select(pd, colsum, bandcol, cls, policy, mass, cost, keep, kept, s);
-  return cuda_status(e);
+  return profile_call(p, Q, K, token_ids, special_ids, n_special, punct_ids, n_punct, nullptr,
+                      policy, mass, cost, colsum, keep, kept, workspace, workspace_bytes,
+                      dev_err, stream);
+}
+
+fg_status fastgen_profile_with_policy(const fg_params* p, const void* Q, const void* K,
+                                      const int32_t* token_ids, const int32_t* special_ids,
+                                      int32_t n_special, const int32_t* punct_ids,
+                                      int32_t n_punct, const int8_t* policy, float* colsum,
+                                      uint8_t* keep, int32_t* kept, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!policy) return FG_EINVAL;
+  return profile_call(p, Q, K, token_ids, special_ids, n_special, punct_ids, n_punct, policy,
+                      nullptr, nullptr, nullptr, colsum, keep, kept, workspace, workspace_bytes,
+                      dev_err, stream);
 }
 
 size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens) {
@@ -261,6 +293,7 @@ fg_status fastgen_read_error(const int32_t* dev_err, void* stream) {
       cudaStreamSynchronize(s) != cudaSuccess)
     return FG_ECUDA;
   if (h & 2) return FG_EDEVICE;
+  if (h & 4) return FG_EINVAL;
   return (h & 1) ? FG_ECAPACITY : FG_OK;
 }
 

@@ -37,17 +37,26 @@ cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void
                                 int ld, float* colsum, float* bandcol, cudaStream_t s);
 
 // The same two passes on the tcgen05 tensor cores (bf16, d = 64 or 128).
-// sched: two ints of scratch (the passes' work counters).  A device-side
-// wait that times out ORs 2 into *err.
+// heads / n_heads (device): when heads is non-null only the *n_heads listed
+// heads are profiled.  sched: two ints of scratch (the passes' work
+// counters).  A device-side wait that times out ORs 2 into *err.
 bool profile_tc_supported(const ProfileDims& pd);
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                              int ld, float* colsum, float* bandcol, int32_t* sched,
-                              int32_t* err, cudaStream_t s);
+                              int ld, float* colsum, float* bandcol, const int32_t* heads,
+                              const int32_t* n_heads, int32_t* sched, int32_t* err,
+                              cudaStream_t s);
 
-// Top-k frequent set, candidate masses, policy, keep codes.
+// Heads whose saved policy contains C_frequent, and their count.
+cudaError_t launch_head_list(const int8_t* fixed, int G, int32_t* heads, int32_t* count,
+                             cudaStream_t s);
+
+// Top-k frequent set, candidate masses, policy, keep codes.  With `fixed`
+// (a saved policy per head) the saved entry is used: mass, cost and policy
+// are not written, and an out-of-range saved value ORs 4 into *err.
 cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,
-                          const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
-                          uint8_t* keep, int32_t* kept, cudaStream_t s);
+                          const uint8_t* cls, const int8_t* fixed, int8_t* policy, float* mass,
+                          int32_t* cost, uint8_t* keep, int32_t* kept, int32_t* err,
+                          cudaStream_t s);
 
 // Per key/value head c: the group policy (largest member policy) and the size
 // of the union of the members' never-evicted prompt sets, as int2 cinfo[c].

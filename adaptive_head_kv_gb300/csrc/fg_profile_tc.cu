@@ -6,7 +6,8 @@
 // A is never written to memory.  Two passes over 128 x 128 score tiles, each
 // a persistent kernel (two CTAs per SM) whose work units are claimed in
 // head-major order from a counter (the tiles of one head run together and
-// share its operands through L2; within a head the longest units go first):
+// share its operands through L2; within a head the longest units go first;
+// with a head list, only the listed heads are profiled):
 //   pass 1, query-major: unit (g, query tile) streams its causal key tiles,
 //     S = Q_tile K_tile^T lands in tensor memory, the consumer warps keep the
 //     running row max and sum and write the negated base-2 row log-sum-exp;
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                       const __grid_constant__ CUtensorMap tmK, float* __restrict__ nlse2,
                       float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
                       int ld, int nt, int w, float sl2, int H, int R,
+                      const int32_t* __restrict__ heads, const int32_t* __restrict__ n_heads,
                       int32_t* __restrict__ sched, int32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& s = *reinterpret_cast<TcSmem<D>*>(
@@ -218,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   volatile int* abort = &s.abort;
   const CUtensorMap* mapA = PASS == 1 ? &tmQ : &tmK;
   const CUtensorMap* mapB = PASS == 1 ? &tmK : &tmQ;
-  const int total_units = G * nt;
 
   if (warp == 0) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -260,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- producer (TMA)
     if (lane == 0) {
+      // every head, or the listed ones (a saved policy map)
+      const int total_units = (heads ? *n_heads : G) * nt;
       int bseq = 0, lseq = 0, ucount = 0;
       int u = atomicAdd(sched, 1);
       while (true) {
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           mbar_arrive(&s.unit_full[us]);
           break;
         }
-        const int g = u / nt, tile = u % nt;
+        const int g = heads ? heads[u / nt] : u / nt, tile = u % nt;
         UnitMeta um;
         um.g = g;
         um.valid = 1;
@@ -510,7 +513,8 @@ int sm_count() {
 
 template <int D>
 cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse2, int ld,
-                float* colsum, float* bandcol, int32_t* sched, int32_t* err, cudaStream_t s) {
+                float* colsum, float* bandcol, const int32_t* heads, const int32_t* n_heads,
+                int32_t* sched, int32_t* err, cudaStream_t s) {
   CUtensorMap tq, tk;
   if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.Gkv, pd.n, D))
     return cudaErrorInvalidValue;
@@ -528,10 +532,11 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
   const unsigned grid = (unsigned)(units < 2LL * sms ? units : 2LL * sms);
   // the work counters were zeroed by the token-class kernel launched before
   e = launch_pdl(profile_tc_kernel<1, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum, bandcol,
-                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, sched, err);
+                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, heads, n_heads, sched, err);
   if (e == cudaSuccess)
     e = launch_pdl(profile_tc_kernel<2, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum,
-                   bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, sched + 1, err);
+                   bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, heads, n_heads,
+                   sched + 1, err);
   return e;
 }
 
@@ -543,10 +548,12 @@ bool profile_tc_supported(const ProfileDims& pd) {
 }
 
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
-                              int ld, float* colsum, float* bandcol, int32_t* sched,
-                              int32_t* err, cudaStream_t s) {
-  return pd.d == 64 ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, sched, err, s)
-                    : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, sched, err, s);
+                              int ld, float* colsum, float* bandcol, const int32_t* heads,
+                              const int32_t* n_heads, int32_t* sched, int32_t* err,
+                              cudaStream_t s) {
+  return pd.d == 64
+             ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s)
+             : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s);
 }
 
 }  // namespace fg

@@ -12,6 +12,9 @@
 //      row i, {i-w < j <= i}, contributes band sums column by column);
 //   3. takes the first shortlist entry with mass >= T (the cheapest, as the
 //      entries are nested) and writes the keep codes of its final cache.
+// With a saved head-policy map (`fixed`), step 3 takes the head's saved
+// entry instead: no masses are formed, and the top-k select runs only for
+// entries containing C_frequent (the only heads the profiler scored).
 #include "fg_common.cuh"
 #include "fg_internal.h"
 
@@ -52,8 +55,9 @@ __device__ __forceinline__ V block_sum(V x, V* red) {
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const float* __restrict__ colsum, const float* __restrict__ bandcol,
     const uint8_t* __restrict__ cls, int n, int HL, int k, int w, float T,
-    int8_t* __restrict__ policy, float* __restrict__ mass, int32_t* __restrict__ cost,
-    uint8_t* __restrict__ keep, int32_t* __restrict__ kept) {
+    const int8_t* __restrict__ fixed, int8_t* __restrict__ policy, float* __restrict__ mass,
+    int32_t* __restrict__ cost, uint8_t* __restrict__ keep, int32_t* __restrict__ kept,
+    int32_t* __restrict__ err) {
   extern __shared__ float cs_smem[];  // the head's colsum when it fits (n <= kSmemN)
   __shared__ unsigned hist[256];
   __shared__ int s_bin, s_krem, s_eq;
@@ -66,8 +70,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   griddep_launch_dependents();
   const int g = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // saved entry of this head (an out-of-range value is recorded and read as full)
+  int saved = -1;
+  if (fixed) {
+    saved = fixed[g];
+    if (saved < FG_POLICY_S || saved > FG_POLICY_FULL) {
+      if (threadIdx.x == 0) atomicOr(err, 4);
+      saved = FG_POLICY_FULL;
+    }
+  }
+  const bool need_f = !fixed || saved == FG_POLICY_SPF || saved == FG_POLICY_SPFL;
   const float* c = colsum + (size_t)g * n;
-  if (n <= kSmemN) {  // read the head's column sums once
+  if (need_f && n <= kSmemN) {  // read the head's column sums once
     for (int j = threadIdx.x; j < n; j += blockDim.x) cs_smem[j] = c[j];
     __syncthreads();
     c = cs_smem;
@@ -75,7 +89,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const float* bc = bandcol + (size_t)g * n;
   const uint8_t* cl = cls + (size_t)(g / HL) * n;
   uint8_t* kp = keep + (size_t)g * n;
-  const bool partial = k > 0 && k < n;
+  const bool partial = need_f && k > 0 && k < n;
 
   // --- 1. radix select of the k-th largest colsum (8-bit digits, MSB first)
   unsigned prefix = 0, mask = 0;
@@ -136,7 +150,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   for (int base = 0; base < n; base += blockDim.x) {
     const int j = base + threadIdx.x;
     const bool valid = j < n;
-    const float cj = valid ? c[j] : 0.f;
+    const float cj = valid && need_f ? c[j] : 0.f;
     const unsigned u = __float_as_uint(cj);
     const int is_eq = (valid && partial && u == thr) ? 1 : 0;
     int eq_rank = 0;
@@ -147,12 +161,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
     if (!valid) continue;
     bool in_f;
-    if (k >= n) in_f = true;
-    else if (k == 0) in_f = false;
+    if (!need_f || k == 0) in_f = false;
+    else if (k >= n) in_f = true;
     else in_f = (u > thr) || (is_eq && (!rank_ties || eq_rank < krem));
     const uint8_t t = cl[j];
     const bool s0 = t & 1, s1 = t != 0, s2 = s1 || in_f, win = j >= n - w;
-    const float bj = bc[j];
+    const float bj = fixed ? 0.f : bc[j];
     if (s0) { a0 += cj; ++c0; }
     if (s1) { a1 += cj; ++c1; }
     if (s2) { a2 += cj; a3 += (double)cj - (double)bj; ++c2; }
@@ -169,13 +183,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const double m[5] = {a0 * inv, a1 * inv, a2 * inv, a3 * inv, 1.0};
     const int cs[5] = {c0, c1, c2, c3, n};
     int p = 4;
-    for (int q = 0; q < 4; ++q)
-      if (m[q] >= (double)T) { p = q; break; }
-    for (int q = 0; q < 5; ++q) {
-      mass[(size_t)g * 5 + q] = (float)m[q];
-      cost[(size_t)g * 5 + q] = cs[q];
+    if (fixed) {
+      p = saved;
+    } else {
+      for (int q = 0; q < 4; ++q)
+        if (m[q] >= (double)T) { p = q; break; }
+      for (int q = 0; q < 5; ++q) {
+        mass[(size_t)g * 5 + q] = (float)m[q];
+        cost[(size_t)g * 5 + q] = cs[q];
+      }
+      policy[g] = (int8_t)p;
     }
-    policy[g] = (int8_t)p;
     kept[g] = cs[p];
     s_policy = p;
   }
@@ -199,7 +217,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
 }
 
+// Heads whose saved entry contains C_frequent (the only ones the profiler
+// scores under a saved map), in increasing order, and their count.  One CTA.
+__global__ void __launch_bounds__(1024) head_list_kernel(const int8_t* __restrict__ fixed, int G,
+                                                         int32_t* __restrict__ heads,
+                                                         int32_t* __restrict__ count) {
+  __shared__ int scratch[33];
+  griddep_wait();
+  griddep_launch_dependents();
+  int base = 0;
+  for (int g0 = 0; g0 < G; g0 += blockDim.x) {
+    const int g = g0 + threadIdx.x;
+    const int p = g < G ? fixed[g] : -1;
+    const int f = (p == FG_POLICY_SPF || p == FG_POLICY_SPFL) ? 1 : 0;
+    int total;
+    const int at = base + block_exclusive_scan(f, scratch, &total);
+    if (f) heads[at] = g;
+    base += total;
+  }
+  if (threadIdx.x == 0) *count = base;
+}
+
 }  // namespace
+
+cudaError_t launch_head_list(const int8_t* fixed, int G, int32_t* heads, int32_t* count,
+                             cudaStream_t s) {
+  return launch_pdl(head_list_kernel, 1, 1024, 0, s, fixed, G, heads, count);
+}
 
 cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
                                const int32_t* punct, int np, uint8_t* cls, int32_t* counters,
@@ -209,8 +253,9 @@ cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* spe
 }
 
 cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const float* bandcol,
-                          const uint8_t* cls, int8_t* policy, float* mass, int32_t* cost,
-                          uint8_t* keep, int32_t* kept, cudaStream_t s) {
+                          const uint8_t* cls, const int8_t* fixed, int8_t* policy, float* mass,
+                          int32_t* cost, uint8_t* keep, int32_t* kept, int32_t* err,
+                          cudaStream_t s) {
   const size_t smem = pd.n <= kSmemN ? (size_t)pd.n * sizeof(float) : 0;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -218,7 +263,7 @@ cudaError_t launch_select(const ProfileDims& pd, const float* colsum, const floa
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(select_kernel, pd.G, kSelThreads, smem, s, colsum, bandcol, cls, pd.n, pd.HL,
-                    pd.k, pd.w, pd.T, policy, mass, cost, keep, kept);
+                    pd.k, pd.w, pd.T, fixed, policy, mass, cost, keep, kept, err);
 }
 
 }  // namespace fg

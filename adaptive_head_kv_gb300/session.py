@@ -6,6 +6,8 @@ kernels.
 """
 from __future__ import annotations
 
+import json
+
 import torch
 
 from . import fastgen as fg
@@ -61,6 +63,20 @@ class FastGenSession:
         fg.fastgen_profile(self.p, Q, K, token_ids, self.special, self.punct, self.policy,
                            self.mass, self.cost, self.colsum, self.keep, self.kept, self.ws,
                            self.dev_err, self.stream)
+
+    def profile_with_policy(self, Q, K, token_ids, policy_map):
+        """Phase 1 under a saved head-policy map (one FG_POLICY_* per query
+        head, host or device): keep codes of each head's saved entry on this
+        prompt; only heads whose entry contains C_frequent are scored."""
+        self.policy.copy_(torch.as_tensor(policy_map, dtype=torch.int8).reshape(-1),
+                          non_blocking=True)
+        fg.fastgen_profile_with_policy(self.p, Q, K, token_ids, self.special, self.punct,
+                                       self.policy, self.colsum, self.keep, self.kept, self.ws,
+                                       self.dev_err, self.stream)
+
+    def prefill_with_policy(self, Q, K, V, token_ids, policy_map):
+        self.profile_with_policy(Q, K, token_ids, policy_map)
+        self.compact(K, V)
 
     def compact(self, K, V):
         self.info = fg.fastgen_compact_plan(self.p, self.policy, self.keep, self.max_new,
@@ -155,3 +171,39 @@ class FastGenSession:
 
         raw = self.plan[: self.Gkv * ctypes.sizeof(fg.HeadDesc)].cpu().numpy().tobytes()
         return (fg.HeadDesc * self.Gkv).from_buffer_copy(raw)
+
+
+POLICY_MAP_FORMAT = "fastgen-head-policy-map"
+
+
+def save_policy_map(path, params: fg.Params, policy) -> None:
+    """Writes a profiled policy (one FG_POLICY_* per query head, flat index
+    g = (b*L + l)*H + h) to a JSON file with the shape it was profiled on."""
+    pol = [int(x) for x in torch.as_tensor(policy).reshape(-1).cpu().tolist()]
+    G = params.B * params.L * params.H
+    if len(pol) != G:
+        raise ValueError(f"policy has {len(pol)} entries, the shape has {G} heads")
+    doc = dict(format=POLICY_MAP_FORMAT, version=1, B=params.B, L=params.L, H=params.H,
+               Hkv=params.Hkv or params.H, n=params.n, T=float(params.T),
+               r_l=float(params.r_l), r_f=float(params.r_f),
+               policies=list(fg.POLICY_NAMES), policy=pol)
+    with open(path, "w") as f:
+        json.dump(doc, f)
+
+
+def load_policy_map(path, params: fg.Params) -> torch.Tensor:
+    """Reads a map written by save_policy_map for the same B, L, H and Hkv
+    (the prompt length may differ); returns int8 [G] on the CPU."""
+    with open(path) as f:
+        doc = json.load(f)
+    if doc.get("format") != POLICY_MAP_FORMAT or doc.get("version") != 1:
+        raise ValueError("not a head-policy map")
+    want = dict(B=params.B, L=params.L, H=params.H, Hkv=params.Hkv or params.H)
+    got = {k: doc.get(k) for k in want}
+    if got != want:
+        raise ValueError(f"map was saved for {got}, the shape is {want}")
+    pol = doc["policy"]
+    if len(pol) != params.B * params.L * params.H or any(not 0 <= p <= 4 for p in pol):
+        raise ValueError("malformed policy list")
+    return torch.tensor(pol, dtype=torch.int8)
+

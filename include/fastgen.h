@@ -11,7 +11,8 @@
  *   2. generation: keep a head-specific cache K_C, V_C = f(K, V, C), append
  *      new keys/values to it by the same policy, and attend over it.
  *
- * The library covers three calls of that path: fastgen_profile (phase 1),
+ * The library covers three calls of that path: fastgen_profile (phase 1;
+ * fastgen_profile_with_policy reuses a saved head-policy map),
  * fastgen_compact_plan + fastgen_compact (building K_C, V_C) and
  * fastgen_decode_attn (one generation step for every head).
  *
@@ -159,6 +160,36 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Phase 1 with a saved head-policy map (policy reuse across prompts: the
+ * overview page's saved head-type map read with the Method's reuse of the
+ * prompt-time policy).
+ *
+ * policy [G] int8 (device, input) fixes each head's shortlist entry
+ * (FG_POLICY_*), e.g. the policy output of an earlier fastgen_profile saved
+ * by the caller.  For this prompt the call writes, per head g, the keep codes
+ * and kept count of that entry's final cache, with the definitions of
+ * fastgen_profile (Spec/Punc from token_ids, the last w positions, the top-k
+ * keys of THIS prompt's colsum).  No masses are formed and no choice is made.
+ * The column sums are computed only for heads whose entry contains
+ * C_frequent (FG_POLICY_SPF, FG_POLICY_SPFL); with bf16 inputs the other heads
+ * skip both profiler passes.  colsum rows of the other heads are left
+ * unspecified (fp32 inputs score every head).
+ *
+ * Arguments as for fastgen_profile, without policy/mass/cost outputs; the
+ * same workspace size.  keep/kept and the policy map then feed
+ * fastgen_compact_plan / fastgen_compact as usual.
+ * A saved value outside 0..4 is read as FG_POLICY_FULL and ORs 4 into
+ * dev_err (fastgen_read_error returns FG_EINVAL).
+ * Errors: those of fastgen_profile; FG_EINVAL for a NULL policy.
+ * ------------------------------------------------------------------------ */
+fg_status fastgen_profile_with_policy(const fg_params* p, const void* Q, const void* K,
+                                      const int32_t* token_ids, const int32_t* special_ids,
+                                      int32_t n_special, const int32_t* punct_ids,
+                                      int32_t n_punct, const int8_t* policy, float* colsum,
+                                      uint8_t* keep, int32_t* kept, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Compaction, step 1: the pool layout (Method: K_C, V_C = f(K, V, C)).
  *
  * From policy [G] and keep [G, n] (outputs of fastgen_profile) it writes,
@@ -258,8 +289,9 @@ fg_status fastgen_decode_attn_noalloc(const fg_params* p, void* plan, const fg_p
                                       int32_t n_punct, int32_t pos, void* out,
                                       int32_t* dev_err, void* stream);
 
-/* Synchronously reads a device flag written by fastgen_profile or
- * fastgen_decode_attn and maps it to a status (FG_OK, FG_ECAPACITY or
+/* Synchronously reads a device flag written by fastgen_profile,
+ * fastgen_profile_with_policy or fastgen_decode_attn and maps it to a status
+ * (FG_OK, FG_ECAPACITY, FG_EINVAL for an out-of-range saved policy, or
  * FG_EDEVICE).  Waits on `stream`. */
 fg_status fastgen_read_error(const int32_t* dev_err, void* stream);
 

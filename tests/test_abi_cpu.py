@@ -65,7 +65,8 @@ def test_workspace_sizes():
     p = P()
     G, n = 6, 100
     al = lambda x: (x + 255) // 256 * 256
-    assert fg.fastgen_profile_workspace_bytes(p) == al(G * 128 * 4) + al(G * n * 4) + al(n) + 256
+    assert fg.fastgen_profile_workspace_bytes(p) == (al(G * 128 * 4) + al(G * n * 4) + al(n) + 256
+                                                     + al(G * 4))
     w = 30
     work = G * ((n + 7 + 255) // 256 + (w + 255) // 256)
     assert fg.fastgen_plan_bytes(p, 7) == al(G * 40) + al(G * 8) + 256 + work * 8
@@ -109,6 +110,41 @@ def test_profile_rejects_pointers_and_workspace():
     assert profile_status(p, ns=-1) == fg.FG_EINVAL
     assert profile_status(p, np_=5000) == fg.FG_EINVAL
     assert profile_status(p, ws_bytes=fg.fastgen_profile_workspace_bytes(p) - 1) == fg.FG_EWORKSPACE
+
+
+def test_profile_with_policy_rejects_on_host():
+    L = fg.lib()
+    p = P()
+
+    def call(pol=FAKE, colsum=FAKE, ws=FAKE, ws_bytes=1 << 40, q=FAKE, **kw):
+        return L.fastgen_profile_with_policy(ctypes.byref(P(**kw) if kw else p), q, FAKE, FAKE,
+                                             FAKE, 1, FAKE, 1, pol, colsum, FAKE, FAKE, ws,
+                                             ws_bytes, FAKE, None)
+
+    assert call(pol=None) == fg.FG_EINVAL
+    assert call(colsum=None) == fg.FG_EINVAL
+    assert call(q=FAKE + 8) == fg.FG_EINVAL
+    assert call(ws=FAKE + 16) == fg.FG_EINVAL
+    assert call(ws_bytes=fg.fastgen_profile_workspace_bytes(p) - 1) == fg.FG_EWORKSPACE
+    assert call(T=0.0) == fg.FG_EINVAL
+    assert call(d=96) == fg.FG_EDTYPE
+
+
+def test_policy_map_json_roundtrip(tmp_path):
+    import torch
+
+    from adaptive_head_kv_gb300.session import load_policy_map, save_policy_map
+
+    p = P(B=2, L=2, H=4, Hkv=2)
+    pol = torch.tensor([0, 1, 2, 3, 4, 4, 3, 2, 1, 0, 0, 2, 3, 1, 4, 2], dtype=torch.int8)
+    path = tmp_path / "map.json"
+    save_policy_map(path, p, pol)
+    got = load_policy_map(path, P(B=2, L=2, H=4, Hkv=2, n=37))  # another prompt length
+    assert torch.equal(got, pol)
+    with pytest.raises(ValueError):
+        load_policy_map(path, P(B=1, L=2, H=4, Hkv=2))
+    with pytest.raises(ValueError):
+        save_policy_map(path, p, pol[:5])
 
 
 def test_plan_compact_decode_reject_on_host():
