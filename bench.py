@@ -290,11 +290,46 @@ def run_ours(args, cfg, rank, world):
     prof_flops = 2.0 * n * (n + 1) * d * G
     kept_rows = int((ckeep != 0).sum())
     comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + Gkv * 40
+    pmap = run_policy_map(args, s, Q, K, V, ids, stream)
     return dict(cfg=cfg, prof_ms=prof_ms, comp_ms=comp_ms, decode_ms=decode_ms, step_ms=step_ms,
                 total_ms=total_ms, dec_ms=dec_ms, dec_bytes=float(dec_bytes_t.mean()),
                 dec_gbs=dec_gbs, prof_flops=prof_flops, comp_bytes=comp_bytes,
-                kept_frac=kept_rows / (Gkv * n), clocks=clk.summary(),
+                kept_frac=kept_rows / (Gkv * n), clocks=clk.summary(), policy_map=pmap,
                 e2e=run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream))
+
+
+def run_policy_map(args, s, Q, K, V, ids, stream):
+    """The prompt phase under a saved head-policy map (the policy just
+    profiled, reused on the same prompt): profile_with_policy + plan +
+    compact, timed like the main loop.  Reported beside the main line; not
+    part of its value."""
+    import torch
+
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    pmap = s.policy.clone()
+    keep0 = s.keep.clone()
+    scored = int(((pmap == fg.FG_POLICY_SPF) | (pmap == fg.FG_POLICY_SPFL)).sum().item())
+    for _ in range(3):
+        s.profile_with_policy(Q, K, ids, pmap)
+        s.compact(K, V)
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(max(args.steps, 3)):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        s.profile_with_policy(Q, K, ids, pmap)
+        e[1].record(stream)
+        s.compact(K, V)
+        e[2].record(stream)
+        per.append(e)
+    torch.cuda.synchronize()
+    assert fg.fastgen_read_error(s.dev_err) == fg.FG_OK
+    same = float((s.keep == keep0).all(dim=1).float().mean().item())
+    prof = float(np.mean([a.elapsed_time(b) for a, b, c in per]))
+    comp = float(np.mean([b.elapsed_time(c) for a, b, c in per]))
+    return dict(profile_ms=prof, compact_plan_ms=comp, scored_heads=scored,
+                heads=int(pmap.numel()), keep_unchanged_fraction=same)
 
 
 def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
@@ -498,6 +533,8 @@ def main():
         "phases_ms": {"profile": r["prof_ms"], "compact_plan": r["comp_ms"],
                       "decode_all_steps": r["decode_ms"], "decode_per_step": dec_launch_ms},
         "kept_fraction": r["kept_frac"],
+        "saved_policy_map": dict(r["policy_map"], prompt_tok_s=world * cfg.B * cfg.n / (
+            (r["policy_map"]["profile_ms"] + r["policy_map"]["compact_plan_ms"]) * 1e-3)),
         "roofline": dominant, "roofline_other": other,
         "clocks": r["clocks"],
         "e2e": {"value": world * cfg.B * cfg.n / (e["prefill_ms"] * 1e-3), "unit": "tok/s",
