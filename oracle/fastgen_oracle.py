@@ -357,3 +357,15 @@ def profile_with_policy(policy, Q, K, ids, special_ids, punct_ids, r_l, r_f, sca
     keep = keep_for_policy(policy, ids, special_ids, punct_ids, r_l, r_f, n, colsum)
     return dict(keep=keep, kept=int((keep != DROP).sum()), colsum=colsum)
 
+
+# --- prompt attention output --------------------------------------------------
+
+def prompt_attention(Q, K, V, scale=None):
+    """The prompt-encoding attention output of one head, O = A V with
+    A = softmax(s Q K^T) under the causal mask (Method, first paragraph and
+    A = softmax(QK^T); reading R1 for s and the mask).  [n, d_v] float64."""
+    Q = np.asarray(Q, dtype=np.float64)
+    s = default_scale(Q.shape[1]) if scale is None else scale
+    A = attention_map(Q, np.asarray(K, dtype=np.float64), s)
+    return A @ np.asarray(V, dtype=np.float64)
+
