@@ -103,9 +103,10 @@ size_t fastgen_profile_workspace_bytes(const fg_params* p) {
          align_up((size_t)p->B * n) + kAlign + align_up(G * sizeof(int32_t));
 }
 
-// Shared by fastgen_profile (fixed == NULL) and fastgen_profile_with_policy.
-static fg_status profile_call(const fg_params* p, const void* Q, const void* K,
-                              const int32_t* token_ids, const int32_t* special_ids,
+// Shared by fastgen_profile (fixed == NULL), fastgen_profile_with_policy and
+// fastgen_profile_attn (V and out non-NULL: the prompt attention output too).
+static fg_status profile_call(const fg_params* p, const void* Q, const void* K, const void* V,
+                              void* out, const int32_t* token_ids, const int32_t* special_ids,
                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
                               const int8_t* fixed, int8_t* policy, float* mass, int32_t* cost,
                               float* colsum, uint8_t* keep, int32_t* kept, void* workspace,
@@ -117,6 +118,8 @@ static fg_status profile_call(const fg_params* p, const void* Q, const void* K,
   if (!Q || !K || !token_ids || !colsum || !keep || !kept || !workspace || !dev_err)
     return FG_EINVAL;
   if (!fixed && (!policy || !mass || !cost)) return FG_EINVAL;
+  if ((V == nullptr) != (out == nullptr)) return FG_EINVAL;
+  if (V && (!aligned(V, 16) || !aligned(out, 16))) return FG_EINVAL;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(workspace, kAlign) ||
       !aligned(colsum, 4) || !aligned(kept, 4) || !aligned(token_ids, 4) ||
       !aligned(dev_err, 4) || (!fixed && (!aligned(mass, 4) || !aligned(cost, 4))))
@@ -148,6 +151,9 @@ static fg_status profile_call(const fg_params* p, const void* Q, const void* K,
     else  // the fp32 path scores every head
       e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
   }
+  if (e == cudaSuccess && V)
+    e = tc ? fg::launch_attn_tc(pd, Q, K, V, lse2, ld, out, sched + 3, dev_err, s)
+           : fg::launch_attn_simt(pd, Q, K, V, lse2, ld, out, s);
   if (e == cudaSuccess)
     e = fg::launch_select(pd, colsum, bandcol, cls, fixed, policy, mass, cost, keep, kept,
                           dev_err, s);
@@ -160,9 +166,21 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           int8_t* policy, float* mass, int32_t* cost, float* colsum,
                           uint8_t* keep, int32_t* kept, void* workspace,
                           size_t workspace_bytes, int32_t* dev_err, void* stream) {
-  return profile_call(p, Q, K, token_ids, special_ids, n_special, punct_ids, n_punct, nullptr,
-                      policy, mass, cost, colsum, keep, kept, workspace, workspace_bytes,
-                      dev_err, stream);
+  return profile_call(p, Q, K, nullptr, nullptr, token_ids, special_ids, n_special, punct_ids,
+                      n_punct, nullptr, policy, mass, cost, colsum, keep, kept, workspace,
+                      workspace_bytes, dev_err, stream);
+}
+
+fg_status fastgen_profile_attn(const fg_params* p, const void* Q, const void* K, const void* V,
+                               const int32_t* token_ids, const int32_t* special_ids,
+                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                               int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                               uint8_t* keep, int32_t* kept, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!V || !out) return FG_EINVAL;
+  return profile_call(p, Q, K, V, out, token_ids, special_ids, n_special, punct_ids, n_punct,
+                      nullptr, policy, mass, cost, colsum, keep, kept, workspace,
+                      workspace_bytes, dev_err, stream);
 }
 
 fg_status fastgen_profile_with_policy(const fg_params* p, const void* Q, const void* K,
@@ -172,9 +190,9 @@ fg_status fastgen_profile_with_policy(const fg_params* p, const void* Q, const v
                                       uint8_t* keep, int32_t* kept, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_err, void* stream) {
   if (!policy) return FG_EINVAL;
-  return profile_call(p, Q, K, token_ids, special_ids, n_special, punct_ids, n_punct, policy,
-                      nullptr, nullptr, nullptr, colsum, keep, kept, workspace, workspace_bytes,
-                      dev_err, stream);
+  return profile_call(p, Q, K, nullptr, nullptr, token_ids, special_ids, n_special, punct_ids,
+                      n_punct, policy, nullptr, nullptr, nullptr, colsum, keep, kept, workspace,
+                      workspace_bytes, dev_err, stream);
 }
 
 size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens) {

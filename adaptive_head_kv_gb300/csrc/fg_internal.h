@@ -23,7 +23,8 @@ struct ProfileDims {
 __host__ __device__ inline int kv_head(int g, int H, int R) { return (g / H) * (H / R) + (g % H) / R; }
 
 // Token class per prompt position: bit 0 special, bit 1 punctuation.  Also
-// zeroes the two work counters of the profiler passes (when non-null).
+// zeroes the work counters of the profiler passes (counters[0], [1] and [3],
+// when non-null).
 cudaError_t launch_token_class(const int32_t* ids, int count, const int32_t* special, int ns,
                                const int32_t* punct, int np, uint8_t* cls, int32_t* counters,
                                cudaStream_t s);
@@ -45,6 +46,15 @@ cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* 
                               int ld, float* colsum, float* bandcol, const int32_t* heads,
                               const int32_t* n_heads, int32_t* sched, int32_t* err,
                               cudaStream_t s);
+
+// Pass 3: the prompt attention output out [G, n, d] = A V, from pass 1's
+// negated base-2 row LSEs.  bf16 on the tensor cores (sched: one zeroed work
+// counter; a timed-out wait ORs 2 into *err), fp32 on SIMT lanes.
+cudaError_t launch_attn_tc(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                           const float* lse2, int ld, void* out, int32_t* sched, int32_t* err,
+                           cudaStream_t s);
+cudaError_t launch_attn_simt(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                             const float* lse2, int ld, void* out, cudaStream_t s);
 
 // Heads whose saved policy contains C_frequent, and their count.
 cudaError_t launch_head_list(const int8_t* fixed, int G, int32_t* heads, int32_t* count,

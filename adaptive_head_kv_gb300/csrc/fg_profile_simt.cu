@@ -197,7 +197,57 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* lse2
   return cudaGetLastError();
 }
 
+// Pass 3: out[g, i] = sum_{j <= i} 2^(s'_ij + lse2_i) v_j, one warp per query
+// row (lanes split d), keys in order.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                   const T* __restrict__ V,
+                                                   const float* __restrict__ lse2, T* __restrict__ out,
+                                                   int n, int ld, float sl2, int H, int R) {
+  constexpr int E = D / 32;
+  const int g = blockIdx.x, i = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const size_t kv = (size_t)kv_head(g, H, R) * n * D;
+  float q[E], acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    q[e] = to_f32(Q[((size_t)g * n + i) * D + lane * E + e]) * sl2;
+    acc[e] = 0.f;
+  }
+  const float nl = lse2[(size_t)g * ld + i];
+  for (int j = 0; j <= i; ++j) {
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) d = fmaf(q[e], to_f32(K[kv + (size_t)j * D + lane * E + e]), d);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    const float p = exp2f(d + nl);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(p, to_f32(V[kv + (size_t)j * D + lane * E + e]), acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) store_out(out + ((size_t)g * n + i) * D + lane * E + e, acc[e]);
+}
+
+template <typename T, int D>
+cudaError_t run_attn(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                     const float* lse2, int ld, void* out, cudaStream_t s) {
+  dim3 grid(pd.G, cdiv(pd.n, 8));
+  attn_kernel<T, D><<<grid, 256, 0, s>>>((const T*)Q, (const T*)K, (const T*)V, lse2, (T*)out,
+                                         pd.n, ld, pd.sl2, pd.H, pd.R);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_attn_simt(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                             const float* lse2, int ld, void* out, cudaStream_t s) {
+  if (pd.dtype == FG_FP32)
+    return pd.d == 64 ? run_attn<float, 64>(pd, Q, K, V, lse2, ld, out, s)
+                      : run_attn<float, 128>(pd, Q, K, V, lse2, ld, out, s);
+  return pd.d == 64 ? run_attn<__nv_bfloat16, 64>(pd, Q, K, V, lse2, ld, out, s)
+                    : run_attn<__nv_bfloat16, 128>(pd, Q, K, V, lse2, ld, out, s);
+}
 
 cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
                                 int ld, float* colsum, float* bandcol, cudaStream_t s) {

@@ -469,6 +469,342 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pass 3: the prompt attention output O = A V (query-major), with the row
+// log-sum-exps of pass 1, so every weight is final when it is formed and the
+// accumulator is never rescaled.  Unit (g, query tile) streams key tiles
+// j <= i: S = Q K^T lands in tensor memory (one buffer), 16 consumer warps
+// (four per TMEM lane quarter, 32 columns each) form P = 2^(s' S + nlse) in
+// bf16 and write it to shared memory in the 128-byte-swizzled K-major layout
+// of an MMA A operand; the MMA warp then accumulates O += P V in tensor
+// memory, V taken straight from its TMA tile as an MN-major B operand.  At
+// the end of a unit the consumers read O (d fp32 columns) and store it.
+// One CTA per SM (the K, V and P rings fill shared memory).
+constexpr int kAttnConsumerWarps = 16;
+constexpr int kAttnTmaWarp = kAttnConsumerWarps, kAttnMmaWarp = kAttnConsumerWarps + 1;
+constexpr int kAttnThreads = (kAttnConsumerWarps + 2) * 32;
+constexpr uint32_t kAttnTmemCols = 256;  // S: columns 0-127, O: 128 .. 128 + d
+constexpr uint32_t kPTileBytes = kBlk * kBlk * 2;
+
+template <int D>
+struct alignas(1024) AttnSmem {
+  uint8_t q[TileCfg<D>::kTileBytes];
+  uint8_t k[kStages][TileCfg<D>::kTileBytes];
+  uint8_t v[kStages][TileCfg<D>::kTileBytes];
+  uint8_t p[2][kPTileBytes];
+  UnitMeta unit[2];
+  int abort;
+  uint64_t a_full, a_empty;
+  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
+  uint64_t s_full, s_empty, pfull[2], pempty[2], o_full, o_empty;
+  uint64_t unit_full[2], unit_empty[2];
+  uint32_t tmem_base;
+};
+
+// Shared-memory descriptor of an MN-major bf16 operand in the 128-byte
+// swizzled layout TMA writes for a [K rows x 64 elements] box: 8-row groups
+// (along K) 1024 bytes apart, 64-element column blocks (along MN) one box
+// (kHalfBytes) apart.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Byte offset of element (row, col) of a 128 x 128 bf16 tile stored as two
+// 64-column halves in the 128-byte swizzled layout.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
+  return (uint32_t)((col >> 6) * (kBlk * 128) + row * 128 +
+                    ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// O += P V over one key tile: P [128 x 128 keys] K-major, V [128 keys x D]
+// MN-major (D of N).
+template <int D>
+__device__ __forceinline__ void issue_pv_mma(uint32_t o_tmem, uint32_t p_base, uint32_t v_base,
+                                             bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlk, D) | (1u << 16);  // B MN-major
+#pragma unroll
+  for (int kk = 0; kk < kBlk / 16; ++kk) {
+    const uint32_t aoff = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
+    const uint32_t boff = kk * 16 * 128;  // 16 key rows of 128 bytes
+    umma_bf16(o_tmem, desc_kmajor_sw128(p_base + aoff),
+              desc_mnmajor_sw128(v_base + boff, TileCfg<D>::kHalfBytes), idesc,
+              (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// nlse2: pass 1's negated base-2 row LSEs (row stride ld); out [G, n, D].
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const float* __restrict__ nlse2,
+                   __nv_bfloat16* __restrict__ out, int G, int n, int ld, int nt, float sl2,
+                   int H, int R, int32_t* __restrict__ sched, int32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem<D>& s = *reinterpret_cast<AttnSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &s.abort;
+
+  if (warp == 0) {
+    tmem_alloc(&s.tmem_base, kAttnTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == kAttnTmaWarp * 32) {
+    s.abort = 0;
+    mbar_init(&s.a_full, 1);
+    mbar_init(&s.a_empty, 1);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.kfull[i], 1);
+      mbar_init(&s.kempty[i], 1);
+      mbar_init(&s.vfull[i], 1);
+      mbar_init(&s.vempty[i], 1);
+    }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_empty, kAttnConsumerWarps);
+    mbar_init(&s.o_full, 1);
+    mbar_init(&s.o_empty, kAttnConsumerWarps);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.pfull[i], kAttnConsumerWarps);
+      mbar_init(&s.pempty[i], 1);
+      mbar_init(&s.unit_full[i], 1);
+      mbar_init(&s.unit_empty[i], kAttnConsumerWarps + 1);
+    }
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  griddep_wait();
+  griddep_launch_dependents();
+
+  if (warp == kAttnTmaWarp) {
+    // ------------------------------------------------------- producer (TMA)
+    if (lane == 0) {
+      const int total_units = G * nt;
+      int kseq = 0, vseq = 0, ucount = 0;
+      int u = atomicAdd(sched, 1);
+      while (true) {
+        const int us = ucount & 1;
+        if (ucount >= 2 && !wait_or_abort(&s.unit_empty[us], ((ucount >> 1) - 1) & 1, abort))
+          break;
+        if (u >= total_units) {
+          s.unit[us].valid = 0;
+          mbar_arrive(&s.unit_full[us]);
+          break;
+        }
+        const int g = u / nt, tile = u % nt;
+        UnitMeta um;
+        um.g = g;
+        um.valid = 1;
+        um.at = nt - 1 - tile;  // longest units first
+        um.b_first = 0;
+        um.nb = um.at + 1;
+        s.unit[us] = um;
+        mbar_arrive(&s.unit_full[us]);
+        const int nxt = atomicAdd(sched, 1);
+        if (ucount >= 1 && !wait_or_abort(&s.a_empty, (ucount - 1) & 1, abort)) break;
+        const int gk = kv_head(g, H, R);
+        mbar_expect_tx(&s.a_full, TileCfg<D>::kTileBytes);
+        load_tile<D>(s.q, &tmQ, &s.a_full, um.at * kBlk, g);
+        bool stop = false;
+        for (int t = 0; t < um.nb && !stop; ++t) {
+          const int ks = kseq % kStages;
+          if (kseq >= kStages && !wait_or_abort(&s.kempty[ks], ((kseq / kStages) - 1) & 1, abort)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(&s.kfull[ks], TileCfg<D>::kTileBytes);
+          load_tile<D>(s.k[ks], &tmK, &s.kfull[ks], t * kBlk, gk);
+          ++kseq;
+          const int vs = vseq % kStages;
+          if (vseq >= kStages && !wait_or_abort(&s.vempty[vs], ((vseq / kStages) - 1) & 1, abort)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(&s.vfull[vs], TileCfg<D>::kTileBytes);
+          load_tile<D>(s.v[vs], &tmV, &s.vfull[vs], t * kBlk, gk);
+          ++vseq;
+        }
+        if (stop) break;
+        ++ucount;
+        u = nxt;
+      }
+      if (*abort) {  // let the copies still in flight land before exiting
+        for (int q = kseq > kStages ? kseq - kStages : 0; q < kseq; ++q)
+          mbar_wait(&s.kfull[q % kStages], (q / kStages) & 1);
+        for (int q = vseq > kStages ? vseq - kStages : 0; q < vseq; ++q)
+          mbar_wait(&s.vfull[q % kStages], (q / kStages) & 1);
+        mbar_wait(&s.a_full, ucount & 1);
+      }
+    }
+  } else if (warp == kAttnMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      int kseq = 0, vseq = 0, sseq = 0, pseq = 0, ucount = 0, ocount = 0, acommits = 0;
+      while (true) {
+        const int us = ucount & 1;
+        if (!wait_or_abort(&s.unit_full[us], (ucount >> 1) & 1, abort)) break;
+        const UnitMeta um = s.unit[us];
+        mbar_arrive(&s.unit_empty[us]);
+        if (!um.valid) break;
+        if (!wait_or_abort(&s.a_full, ucount & 1, abort)) break;
+        bool stop = false;
+        for (int t = 0; t <= um.nb && !stop; ++t) {
+          if (t < um.nb) {  // scores of key tile t
+            const int ks = kseq % kStages;
+            if (!wait_or_abort(&s.kfull[ks], (kseq / kStages) & 1, abort) ||
+                (sseq >= 1 && !wait_or_abort(&s.s_empty, (sseq - 1) & 1, abort))) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            issue_tile_mma<D>(tmem, smem_addr(s.q), smem_addr(s.k[ks]));
+            umma_commit(&s.s_full);
+            umma_commit(&s.kempty[ks]);
+            ++kseq;
+            ++sseq;
+          }
+          if (t >= 1) {  // weighted values of key tile t - 1
+            const int pb = pseq & 1, vs = vseq % kStages;
+            if (!wait_or_abort(&s.pfull[pb], (pseq >> 1) & 1, abort) ||
+                !wait_or_abort(&s.vfull[vs], (vseq / kStages) & 1, abort) ||
+                (t == 1 && ocount >= 1 && !wait_or_abort(&s.o_empty, (ocount - 1) & 1, abort))) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            issue_pv_mma<D>(tmem + kBlk, smem_addr(s.p[pb]), smem_addr(s.v[vs]), t > 1);
+            umma_commit(&s.pempty[pb]);
+            umma_commit(&s.vempty[vs]);
+            ++pseq;
+            ++vseq;
+          }
+        }
+        if (stop) break;
+        umma_commit(&s.o_full);
+        ++ocount;
+        umma_commit(&s.a_empty);
+        ++acommits;
+        ++ucount;
+      }
+      // every MMA issued must complete before exit; the last commits cover them
+      if (acommits > 0) mbar_wait(&s.a_empty, (acommits - 1) & 1);
+      for (int q = kseq > kStages ? kseq - kStages : 0; q < kseq; ++q)
+        mbar_wait(&s.kempty[q % kStages], (q / kStages) & 1);
+      for (int q = vseq > kStages ? vseq - kStages : 0; q < vseq; ++q)
+        mbar_wait(&s.vempty[q % kStages], (q / kStages) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    // warp w reads TMEM lanes 32*(w%4).. (its rows), S columns 32*(w/4)..
+    // and O columns 32*(w/4).. (those below D)
+    const int qd = warp & 3, cg = warp >> 2;
+    const int row = qd * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    int sseq = 0, pseq = 0, ucount = 0;
+    while (true) {
+      const int us = ucount & 1;
+      if (!wait_or_abort(&s.unit_full[us], (ucount >> 1) & 1, abort)) break;
+      const UnitMeta um = s.unit[us];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.unit_empty[us]);
+      if (!um.valid) break;
+      const int qpos = um.at * kBlk + row;                   // query position
+      const float nl = nlse2[(size_t)um.g * ld + qpos];      // -inf past the prompt
+      bool stop = false;
+      for (int t = 0; t < um.nb; ++t) {
+        if (!wait_or_abort(&s.s_full, sseq & 1, abort)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(lane_base + cg * 32, r);
+        tmem_wait_ld(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.s_empty);
+        ++sseq;
+        // keys t*128 + cg*32 + e count for key <= query and key < n
+        const int lim = min(qpos + 1, n) - (t * kBlk + cg * 32);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = e < lim ? ex2(fmaf(f(r[e]), sl2, nl)) : 0.f;
+          const float p1 = e + 1 < lim ? ex2(fmaf(f(r[e + 1]), sl2, nl)) : 0.f;
+          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        const int pb = pseq & 1;
+        if (pseq >= 2 && !wait_or_abort(&s.pempty[pb], ((pseq >> 1) - 1) & 1, abort)) {
+          stop = true;
+          break;
+        }
+        uint8_t* pt = s.p[pb];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(pt + sw128_offset(row, cg * 32 + c * 8)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async_smem();  // generic writes, read next by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.pfull[pb]);
+        ++pseq;
+      }
+      if (stop) break;
+      // the unit's output rows
+      if (!wait_or_abort(&s.o_full, ucount & 1, abort)) break;
+      tc_fence_after();
+      uint32_t o[32];
+      if (cg * 32 < D) {  // D = 64: the warps of column groups 0 and 1 read 32 columns each
+        const int c0 = cg * 32;
+        tmem_ld32(lane_base + kBlk + c0, o);
+        tmem_wait_ld(o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.o_empty);
+        if (qpos < n) {
+          __nv_bfloat16* dst = out + ((size_t)um.g * n + qpos) * D + c0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(f(o[8 * c + 2 * e]), f(o[8 * c + 2 * e + 1]));
+              w4[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.o_empty);
+      }
+      ++ucount;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s.abort) atomicOr(err, 2);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAttnTmemCols);
+  }
+}
+
 using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
 
 EncodeFn encoder() {
@@ -540,6 +876,27 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
   return e;
 }
 
+template <int D>
+cudaError_t run_attn(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                     const float* nlse2, int ld, void* out, int32_t* sched, int32_t* err,
+                     cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.Gkv, pd.n, D) ||
+      !make_map(&tv, V, pd.Gkv, pd.n, D))
+    return cudaErrorInvalidValue;
+  const int nt = cdiv(pd.n, kBlk);
+  const size_t smem = sizeof(AttnSmem<D>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)pd.G * nt;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
+  return launch_pdl(attn_tc_kernel<D>, grid, kAttnThreads, smem, s, tq, tk, tv, nlse2,
+                    (__nv_bfloat16*)out, pd.G, pd.n, ld, nt, pd.sl2, pd.H, pd.R, sched, err);
+}
+
 }  // namespace
 
 bool profile_tc_supported(const ProfileDims& pd) {
@@ -554,6 +911,13 @@ cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* 
   return pd.d == 64
              ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s)
              : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s);
+}
+
+cudaError_t launch_attn_tc(const ProfileDims& pd, const void* Q, const void* K, const void* V,
+                           const float* lse2, int ld, void* out, int32_t* sched, int32_t* err,
+                           cudaStream_t s) {
+  return pd.d == 64 ? run_attn<64>(pd, Q, K, V, lse2, ld, out, sched, err, s)
+                    : run_attn<128>(pd, Q, K, V, lse2, ld, out, sched, err, s);
 }
 
 }  // namespace fg

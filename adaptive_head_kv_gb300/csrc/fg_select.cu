@@ -31,7 +31,7 @@ __global__ void token_class_kernel(const int32_t* __restrict__ ids, int count,
   griddep_wait();
   griddep_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i == 0 && counters) counters[0] = counters[1] = 0;  // the profiler passes' work counters
+  if (i == 0 && counters) counters[0] = counters[1] = counters[3] = 0;  // passes' work counters
   if (i >= count) return;
   const int id = ids[i];
   cls[i] = (uint8_t)((id_in(id, special, ns) ? 1 : 0) | (id_in(id, punct, np) ? 2 : 0));

@@ -22,13 +22,14 @@ POLICY_NAMES = ("special", "special+punct", "special+punct+frequent",
 FG_KEEP_DROP, FG_KEEP_STATIC, FG_KEEP_WINDOW = 0, 1, 2
 
 # kernels launched by one call of each entry point (counted in the bench)
-LAUNCHES = {"profile": 4, "profile_with_policy": 5, "plan": 3, "compact": 1, "decode": 2}
+LAUNCHES = {"profile": 4, "profile_attn": 5, "profile_with_policy": 5, "plan": 3, "compact": 1,
+            "decode": 2}
 
 EXPORTS = (
     "fastgen_status_string", "fastgen_version", "fastgen_profile_workspace_bytes",
     "fastgen_profile", "fastgen_plan_bytes", "fastgen_compact_plan", "fastgen_compact",
     "fastgen_decode_workspace_bytes", "fastgen_decode_attn", "fastgen_read_error",
-    "fastgen_decode_attn_noalloc", "fastgen_profile_with_policy",
+    "fastgen_decode_attn_noalloc", "fastgen_profile_with_policy", "fastgen_profile_attn",
 )
 
 # size of the library-held scratch array used by fastgen_decode_attn_noalloc
@@ -71,6 +72,8 @@ _SIGS = {
                                        _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "fastgen_profile_with_policy": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, _I32,
                                                    _P, _I32, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "fastgen_profile_attn": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _I32, _P,
+                                            _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "fastgen_plan_bytes": (_SZ, [ctypes.POINTER(Params), _I32]),
     "fastgen_compact_plan": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _I32, _P, _SZ,
                                             ctypes.POINTER(PlanInfo), _P]),
@@ -164,6 +167,16 @@ def fastgen_profile_with_policy(params, Q, K, token_ids, special_ids, punct_ids,
         _count(special_ids), _ptr(punct_ids), _count(punct_ids), _ptr(policy), _ptr(colsum),
         _ptr(keep), _ptr(kept), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
         "fastgen_profile_with_policy")
+
+
+def fastgen_profile_attn(params, Q, K, V, token_ids, special_ids, punct_ids, policy, mass, cost,
+                         colsum, keep, kept, out, workspace, dev_err, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    _check(lib().fastgen_profile_attn(
+        ctypes.byref(params), _ptr(Q), _ptr(K), _ptr(V), _ptr(token_ids), _ptr(special_ids),
+        _count(special_ids), _ptr(punct_ids), _count(punct_ids), _ptr(policy), _ptr(mass),
+        _ptr(cost), _ptr(colsum), _ptr(keep), _ptr(kept), _ptr(out), _ptr(workspace), ws_bytes,
+        _ptr(dev_err), _stream(stream)), "fastgen_profile_attn")
 
 
 def fastgen_plan_bytes(params: Params, max_new_tokens: int) -> int:

@@ -64,6 +64,13 @@ class FastGenSession:
                            self.mass, self.cost, self.colsum, self.keep, self.kept, self.ws,
                            self.dev_err, self.stream)
 
+    def profile_attn(self, Q, K, V, token_ids, out):
+        """profile() plus the prompt attention output out [G, n, d] = A V."""
+        fg.fastgen_profile_attn(self.p, Q, K, V, token_ids, self.special, self.punct,
+                                self.policy, self.mass, self.cost, self.colsum, self.keep,
+                                self.kept, out, self.ws, self.dev_err, self.stream)
+        return out
+
     def profile_with_policy(self, Q, K, token_ids, policy_map):
         """Phase 1 under a saved head-policy map (one FG_POLICY_* per query
         head, host or device): keep codes of each head's saved entry on this

@@ -12,6 +12,7 @@
  *      new keys/values to it by the same policy, and attend over it.
  *
  * The library covers three calls of that path: fastgen_profile (phase 1;
+ * fastgen_profile_attn also returns the prompt attention output,
  * fastgen_profile_with_policy reuses a saved head-policy map),
  * fastgen_compact_plan + fastgen_compact (building K_C, V_C) and
  * fastgen_decode_attn (one generation step for every head).
@@ -158,6 +159,27 @@ fg_status fastgen_profile(const fg_params* p, const void* Q, const void* K,
                           int8_t* policy, float* mass, int32_t* cost, float* colsum,
                           uint8_t* keep, int32_t* kept, void* workspace,
                           size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Phase 1 with the prompt attention output (Method, first paragraph: the
+ * prompt-encoding phase runs attention over the prompt; A = softmax(QK^T)).
+ *
+ * Everything fastgen_profile writes, plus
+ *   out[g, i, :] = sum_{j <= i} A_ij v_j        (V [Gkv, n, d] like K)
+ * for every query head g and prompt position i, in the dtype of Q/K/V,
+ * row-major [G, n, d], 16-byte aligned.  A third pass reuses the row
+ * log-sum-exps of the first, so each weight A_ij is final when it is formed
+ * (no rescaling); bf16 inputs run it on the tcgen05 tensor cores (P rounded
+ * to bf16 for the P V product, fp32 accumulation), fp32 inputs on fp32 SIMT
+ * arithmetic.  Same workspace as fastgen_profile.
+ * Errors: those of fastgen_profile; FG_EINVAL for NULL or misaligned V/out.
+ * ------------------------------------------------------------------------ */
+fg_status fastgen_profile_attn(const fg_params* p, const void* Q, const void* K, const void* V,
+                               const int32_t* token_ids, const int32_t* special_ids,
+                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                               int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                               uint8_t* keep, int32_t* kept, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Phase 1 with a saved head-policy map (policy reuse across prompts: the
