@@ -291,10 +291,12 @@ def run_ours(args, cfg, rank, world):
     kept_rows = int((ckeep != 0).sum())
     comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + Gkv * 40
     pmap = run_policy_map(args, s, Q, K, V, ids, stream)
+    pattn = run_prompt_attention(args, s, cfg, Q, K, V, ids, stream)
     return dict(cfg=cfg, prof_ms=prof_ms, comp_ms=comp_ms, decode_ms=decode_ms, step_ms=step_ms,
                 total_ms=total_ms, dec_ms=dec_ms, dec_bytes=float(dec_bytes_t.mean()),
                 dec_gbs=dec_gbs, prof_flops=prof_flops, comp_bytes=comp_bytes,
                 kept_frac=kept_rows / (Gkv * n), clocks=clk.summary(), policy_map=pmap,
+                prompt_attention=pattn,
                 e2e=run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream))
 
 
@@ -330,6 +332,40 @@ def run_policy_map(args, s, Q, K, V, ids, stream):
     comp = float(np.mean([b.elapsed_time(c) for a, b, c in per]))
     return dict(profile_ms=prof, compact_plan_ms=comp, scored_heads=scored,
                 heads=int(pmap.numel()), keep_unchanged_fraction=same)
+
+
+def run_prompt_attention(args, s, cfg, Q, K, V, ids, stream):
+    """fastgen_profile_attn (the profile plus the prompt attention output
+    A V) against fastgen_profile on the same prompt; the difference is the
+    attention-output pass.  Reported beside the main line."""
+    import torch
+
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    out = torch.empty((cfg.G, cfg.n, cfg.d), dtype=s.tdtype, device=Q.device)
+    for _ in range(3):
+        s.profile_attn(Q, K, V, ids, out)
+        s.profile(Q, K, ids)
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(max(args.steps, 3)):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        s.profile_attn(Q, K, V, ids, out)
+        e[1].record(stream)
+        s.profile(Q, K, ids)
+        e[2].record(stream)
+        per.append(e)
+    torch.cuda.synchronize()
+    assert fg.fastgen_read_error(s.dev_err) == fg.FG_OK
+    with_attn = float(np.mean([a.elapsed_time(b) for a, b, c in per]))
+    plain = float(np.mean([b.elapsed_time(c) for a, b, c in per]))
+    attn_ms = with_attn - plain
+    # causal Q K^T and P V: 2 * d * n(n+1)/2 flops each per head
+    flops = 2.0 * cfg.d * cfg.n * (cfg.n + 1) * cfg.G
+    del out
+    return dict(profile_attn_ms=with_attn, profile_ms=plain, attention_pass_ms=attn_ms,
+                attention_pass_tflops=flops / (attn_ms * 1e-3) / 1e12 if attn_ms > 0 else None)
 
 
 def run_e2e(args, s, cfg, hQ, hK, hV, hids, hq, hk, hv, hdec_ids, stream):
@@ -535,6 +571,7 @@ def main():
         "kept_fraction": r["kept_frac"],
         "saved_policy_map": dict(r["policy_map"], prompt_tok_s=world * cfg.B * cfg.n / (
             (r["policy_map"]["profile_ms"] + r["policy_map"]["compact_plan_ms"]) * 1e-3)),
+        "prompt_attention_output": r["prompt_attention"],
         "roofline": dominant, "roofline_other": other,
         "clocks": r["clocks"],
         "e2e": {"value": world * cfg.B * cfg.n / (e["prefill_ms"] * 1e-3), "unit": "tok/s",
