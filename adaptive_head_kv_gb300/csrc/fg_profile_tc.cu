@@ -473,30 +473,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Pass 3: the prompt attention output O = A V (query-major), with the row
 // log-sum-exps of pass 1, so every weight is final when it is formed and the
 // accumulator is never rescaled.  Unit (g, query tile) streams key tiles
-// j <= i: S = Q K^T lands in tensor memory (one buffer), 16 consumer warps
+// j <= i: S = Q K^T lands in tensor memory (two buffers), 16 consumer warps
 // (four per TMEM lane quarter, 32 columns each) form P = 2^(s' S + nlse) in
 // bf16 and write it to shared memory in the 128-byte-swizzled K-major layout
 // of an MMA A operand; the MMA warp then accumulates O += P V in tensor
 // memory, V taken straight from its TMA tile as an MN-major B operand.  At
-// the end of a unit the consumers read O (d fp32 columns) and store it.
-// One CTA per SM (the K, V and P rings fill shared memory).
+// the end of a unit the consumers read O (d fp32 columns) and store it.  The
+// query tile is double-buffered so the next unit's loads during this one.
+// One CTA per SM (the Q, K, V and P buffers fill shared memory).
 constexpr int kAttnConsumerWarps = 16;
 constexpr int kAttnTmaWarp = kAttnConsumerWarps, kAttnMmaWarp = kAttnConsumerWarps + 1;
 constexpr int kAttnThreads = (kAttnConsumerWarps + 2) * 32;
-constexpr uint32_t kAttnTmemCols = 256;  // S: columns 0-127, O: 128 .. 128 + d
+constexpr uint32_t kAttnTmemCols = 512;  // S: two buffers at columns 0 and 128, O at 256
+constexpr uint32_t kAttnOCol = 2 * kBlk;
 constexpr uint32_t kPTileBytes = kBlk * kBlk * 2;
 
 template <int D>
 struct alignas(1024) AttnSmem {
-  uint8_t q[TileCfg<D>::kTileBytes];
+  uint8_t q[2][TileCfg<D>::kTileBytes];  // this unit's and the next unit's queries
   uint8_t k[kStages][TileCfg<D>::kTileBytes];
   uint8_t v[kStages][TileCfg<D>::kTileBytes];
-  uint8_t p[2][kPTileBytes];
+  uint8_t p[kPTileBytes];
   UnitMeta unit[2];
   int abort;
-  uint64_t a_full, a_empty;
+  uint64_t a_full[2], a_empty[2];
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s_full, s_empty, pfull[2], pempty[2], o_full, o_empty;
+  uint64_t s_full[2], s_empty[2], pfull, pempty, o_full, o_empty;
   uint64_t unit_full[2], unit_empty[2];
   uint32_t tmem_base;
 };
@@ -561,8 +563,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (threadIdx.x == kAttnTmaWarp * 32) {
     s.abort = 0;
-    mbar_init(&s.a_full, 1);
-    mbar_init(&s.a_empty, 1);
 #pragma unroll
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.kfull[i], 1);
@@ -570,14 +570,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&s.vfull[i], 1);
       mbar_init(&s.vempty[i], 1);
     }
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.s_empty, kAttnConsumerWarps);
+    mbar_init(&s.pfull, kAttnConsumerWarps);
+    mbar_init(&s.pempty, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.o_empty, kAttnConsumerWarps);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.pfull[i], kAttnConsumerWarps);
-      mbar_init(&s.pempty[i], 1);
+      mbar_init(&s.a_full[i], 1);
+      mbar_init(&s.a_empty[i], 1);
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_empty[i], kAttnConsumerWarps);
       mbar_init(&s.unit_full[i], 1);
       mbar_init(&s.unit_empty[i], kAttnConsumerWarps + 1);
     }
@@ -615,10 +617,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         s.unit[us] = um;
         mbar_arrive(&s.unit_full[us]);
         const int nxt = atomicAdd(sched, 1);
-        if (ucount >= 1 && !wait_or_abort(&s.a_empty, (ucount - 1) & 1, abort)) break;
+        // the query tile of the unit two back must be released
+        if (ucount >= 2 && !wait_or_abort(&s.a_empty[us], ((ucount >> 1) - 1) & 1, abort)) break;
         const int gk = kv_head(g, H, R);
-        mbar_expect_tx(&s.a_full, TileCfg<D>::kTileBytes);
-        load_tile<D>(s.q, &tmQ, &s.a_full, um.at * kBlk, g);
+        mbar_expect_tx(&s.a_full[us], TileCfg<D>::kTileBytes);
+        load_tile<D>(s.q[us], &tmQ, &s.a_full[us], um.at * kBlk, g);
         bool stop = false;
         for (int t = 0; t < um.nb && !stop; ++t) {
           const int ks = kseq % kStages;
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_wait(&s.kfull[q % kStages], (q / kStages) & 1);
         for (int q = vseq > kStages ? vseq - kStages : 0; q < vseq; ++q)
           mbar_wait(&s.vfull[q % kStages], (q / kStages) & 1);
-        mbar_wait(&s.a_full, ucount & 1);
+        mbar_wait(&s.a_full[ucount & 1], (ucount >> 1) & 1);
       }
     }
   } else if (warp == kAttnMmaWarp) {
@@ -660,34 +663,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const UnitMeta um = s.unit[us];
         mbar_arrive(&s.unit_empty[us]);
         if (!um.valid) break;
-        if (!wait_or_abort(&s.a_full, ucount & 1, abort)) break;
+        if (!wait_or_abort(&s.a_full[us], (ucount >> 1) & 1, abort)) break;
         bool stop = false;
         for (int t = 0; t <= um.nb && !stop; ++t) {
           if (t < um.nb) {  // scores of key tile t
-            const int ks = kseq % kStages;
+            const int ks = kseq % kStages, sb = sseq & 1;
             if (!wait_or_abort(&s.kfull[ks], (kseq / kStages) & 1, abort) ||
-                (sseq >= 1 && !wait_or_abort(&s.s_empty, (sseq - 1) & 1, abort))) {
+                (sseq >= 2 && !wait_or_abort(&s.s_empty[sb], ((sseq >> 1) - 1) & 1, abort))) {
               stop = true;
               break;
             }
             tc_fence_after();
-            issue_tile_mma<D>(tmem, smem_addr(s.q), smem_addr(s.k[ks]));
-            umma_commit(&s.s_full);
+            issue_tile_mma<D>(tmem + sb * kBlk, smem_addr(s.q[us]), smem_addr(s.k[ks]));
+            umma_commit(&s.s_full[sb]);
             umma_commit(&s.kempty[ks]);
             ++kseq;
             ++sseq;
           }
           if (t >= 1) {  // weighted values of key tile t - 1
-            const int pb = pseq & 1, vs = vseq % kStages;
-            if (!wait_or_abort(&s.pfull[pb], (pseq >> 1) & 1, abort) ||
+            const int vs = vseq % kStages;
+            if (!wait_or_abort(&s.pfull, pseq & 1, abort) ||
                 !wait_or_abort(&s.vfull[vs], (vseq / kStages) & 1, abort) ||
                 (t == 1 && ocount >= 1 && !wait_or_abort(&s.o_empty, (ocount - 1) & 1, abort))) {
               stop = true;
               break;
             }
             tc_fence_after();
-            issue_pv_mma<D>(tmem + kBlk, smem_addr(s.p[pb]), smem_addr(s.v[vs]), t > 1);
-            umma_commit(&s.pempty[pb]);
+            issue_pv_mma<D>(tmem + kAttnOCol, smem_addr(s.p), smem_addr(s.v[vs]), t > 1);
+            umma_commit(&s.pempty);
             umma_commit(&s.vempty[vs]);
             ++pseq;
             ++vseq;
@@ -696,12 +699,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (stop) break;
         umma_commit(&s.o_full);
         ++ocount;
-        umma_commit(&s.a_empty);
+        umma_commit(&s.a_empty[us]);
         ++acommits;
         ++ucount;
       }
       // every MMA issued must complete before exit; the last commits cover them
-      if (acommits > 0) mbar_wait(&s.a_empty, (acommits - 1) & 1);
+      if (acommits > 0) mbar_wait(&s.a_empty[(acommits - 1) & 1], ((acommits - 1) >> 1) & 1);
       for (int q = kseq > kStages ? kseq - kStages : 0; q < kseq; ++q)
         mbar_wait(&s.kempty[q % kStages], (q / kStages) & 1);
       for (int q = vseq > kStages ? vseq - kStages : 0; q < vseq; ++q)
@@ -726,17 +729,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float nl = nlse2[(size_t)um.g * ld + qpos];      // -inf past the prompt
       bool stop = false;
       for (int t = 0; t < um.nb; ++t) {
-        if (!wait_or_abort(&s.s_full, sseq & 1, abort)) {
+        const int sb = sseq & 1;
+        if (!wait_or_abort(&s.s_full[sb], (sseq >> 1) & 1, abort)) {
           stop = true;
           break;
         }
         tc_fence_after();
         uint32_t r[32];
-        tmem_ld32(lane_base + cg * 32, r);
+        tmem_ld32(lane_base + sb * kBlk + cg * 32, r);
         tmem_wait_ld(r);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_empty);
+        if (lane == 0) mbar_arrive(&s.s_empty[sb]);
         ++sseq;
         // keys t*128 + cg*32 + e count for key <= query and key < n
         const int lim = min(qpos + 1, n) - (t * kBlk + cg * 32);
@@ -748,19 +752,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
           pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h);
         }
-        const int pb = pseq & 1;
-        if (pseq >= 2 && !wait_or_abort(&s.pempty[pb], ((pseq >> 1) - 1) & 1, abort)) {
+        if (pseq >= 1 && !wait_or_abort(&s.pempty, (pseq - 1) & 1, abort)) {
           stop = true;
           break;
         }
-        uint8_t* pt = s.p[pb];
+        uint8_t* pt = s.p;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(pt + sw128_offset(row, cg * 32 + c * 8)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         fence_proxy_async_smem();  // generic writes, read next by the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.pfull[pb]);
+        if (lane == 0) mbar_arrive(&s.pfull);
         ++pseq;
       }
       if (stop) break;
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t o[32];
       if (cg * 32 < D) {  // D = 64: the warps of column groups 0 and 1 read 32 columns each
         const int c0 = cg * 32;
-        tmem_ld32(lane_base + kBlk + c0, o);
+        tmem_ld32(lane_base + kAttnOCol + c0, o);
         tmem_wait_ld(o);
         tc_fence_before();
         __syncwarp();
