@@ -524,6 +524,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
                     ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
+// (lo, hi) -> bf16x2, lo in the low half, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -745,12 +752,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // keys t*128 + cg*32 + e count for key <= query and key < n
         const int lim = min(qpos + 1, n) - (t * kBlk + cg * 32);
         uint32_t pk[16];
+        if (lim >= 32) {  // every key of the chunk counts: packed arithmetic, no tests
+          const uint64_t s2 = pack2(sl2, sl2), nl2 = pack2(nl, nl);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = e < lim ? ex2(fmaf(f(r[e]), sl2, nl)) : 0.f;
-          const float p1 = e + 1 < lim ? ex2(fmaf(f(r[e + 1]), sl2, nl)) : 0.f;
-          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h);
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1;
+            unpack2(fma2(pack2(f(r[e]), f(r[e + 1])), s2, nl2), x0, x1);
+            pk[e >> 1] = pack_bf16x2_rn(ex2(x0), ex2(x1));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = e < lim ? ex2(fmaf(f(r[e]), sl2, nl)) : 0.f;
+            const float p1 = e + 1 < lim ? ex2(fmaf(f(r[e + 1]), sl2, nl)) : 0.f;
+            pk[e >> 1] = pack_bf16x2_rn(p0, p1);
+          }
         }
         if (pseq >= 1 && !wait_or_abort(&s.pempty, (pseq - 1) & 1, abort)) {
           stop = true;
