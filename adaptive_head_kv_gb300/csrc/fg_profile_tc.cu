@@ -475,30 +475,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 // accumulator is never rescaled.  Unit (g, query tile) streams key tiles
 // j <= i: S = Q K^T lands in tensor memory (two buffers), 16 consumer warps
 // (four per TMEM lane quarter, 32 columns each) form P = 2^(s' S + nlse) in
-// bf16 and write it to shared memory in the 128-byte-swizzled K-major layout
-// of an MMA A operand; the MMA warp then accumulates O += P V in tensor
-// memory, V taken straight from its TMA tile as an MN-major B operand.  At
+// bf16 and store it back to tensor memory (two P buffers; row = lane, key
+// pairs packed per column), where the MMA warp takes it as the A operand of
+// O += P V, V read straight from its TMA tile as an MN-major B operand.  At
 // the end of a unit the consumers read O (d fp32 columns) and store it.  The
 // query tile is double-buffered so the next unit's loads during this one.
-// One CTA per SM (the Q, K, V and P buffers fill shared memory).
+// One CTA per SM (the Q, K and V buffers fill shared memory).
 constexpr int kAttnConsumerWarps = 16;
 constexpr int kAttnTmaWarp = kAttnConsumerWarps, kAttnMmaWarp = kAttnConsumerWarps + 1;
 constexpr int kAttnThreads = (kAttnConsumerWarps + 2) * 32;
-constexpr uint32_t kAttnTmemCols = 512;  // S: two buffers at columns 0 and 128, O at 256
+// tensor memory: S buffers at columns 0 and 128, O at 256, P buffers at 384, 448
+constexpr uint32_t kAttnTmemCols = 512;
 constexpr uint32_t kAttnOCol = 2 * kBlk;
-constexpr uint32_t kPTileBytes = kBlk * kBlk * 2;
+constexpr uint32_t kAttnPCol = 3 * kBlk;
 
 template <int D>
 struct alignas(1024) AttnSmem {
   uint8_t q[2][TileCfg<D>::kTileBytes];  // this unit's and the next unit's queries
   uint8_t k[kStages][TileCfg<D>::kTileBytes];
   uint8_t v[kStages][TileCfg<D>::kTileBytes];
-  uint8_t p[kPTileBytes];
   UnitMeta unit[2];
   int abort;
   uint64_t a_full[2], a_empty[2];
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s_full[2], s_empty[2], pfull, pempty, o_full, o_empty;
+  uint64_t s_full[2], s_empty[2], pfull[2], pempty[2], o_full, o_empty;
   uint64_t unit_full[2], unit_empty[2];
   uint32_t tmem_base;
 };
@@ -517,13 +517,6 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
   return d;
 }
 
-// Byte offset of element (row, col) of a 128 x 128 bf16 tile stored as two
-// 64-column halves in the 128-byte swizzled layout.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
-  return (uint32_t)((col >> 6) * (kBlk * 128) + row * 128 +
-                    ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
-}
-
 // (lo, hi) -> bf16x2, lo in the low half, round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   uint32_t r;
@@ -531,24 +524,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand read from tensor memory (its
+// rows on the lanes, two bf16 per 32-bit column along K).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-// O += P V over one key tile: P [128 x 128 keys] K-major, V [128 keys x D]
-// MN-major (D of N).
+// 16 consecutive 32-bit columns of this thread's TMEM lane (32x32b shape).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// O += P V over one key tile: P [128 x 128 keys] in tensor memory (64
+// columns), V [128 keys x D] MN-major in shared memory (D of N).
 template <int D>
-__device__ __forceinline__ void issue_pv_mma(uint32_t o_tmem, uint32_t p_base, uint32_t v_base,
+__device__ __forceinline__ void issue_pv_mma(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_base,
                                              bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlk, D) | (1u << 16);  // B MN-major
 #pragma unroll
-  for (int kk = 0; kk < kBlk / 16; ++kk) {
-    const uint32_t aoff = (kk >> 2) * (kBlk * 128) + (kk & 3) * 32;
-    const uint32_t boff = kk * 16 * 128;  // 16 key rows of 128 bytes
-    umma_bf16(o_tmem, desc_kmajor_sw128(p_base + aoff),
-              desc_mnmajor_sw128(v_base + boff, TileCfg<D>::kHalfBytes), idesc,
-              (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kBlk / 16; ++kk)
+    umma_bf16_ts(o_tmem, p_tmem + kk * 8,
+                 desc_mnmajor_sw128(v_base + kk * 16 * 128, TileCfg<D>::kHalfBytes), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // nlse2: pass 1's negated base-2 row LSEs (row stride ld); out [G, n, D].
@@ -577,8 +590,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&s.vfull[i], 1);
       mbar_init(&s.vempty[i], 1);
     }
-    mbar_init(&s.pfull, kAttnConsumerWarps);
-    mbar_init(&s.pempty, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.o_empty, kAttnConsumerWarps);
 #pragma unroll
@@ -587,6 +598,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&s.a_empty[i], 1);
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.s_empty[i], kAttnConsumerWarps);
+      mbar_init(&s.pfull[i], kAttnConsumerWarps);
+      mbar_init(&s.pempty[i], 1);
       mbar_init(&s.unit_full[i], 1);
       mbar_init(&s.unit_empty[i], kAttnConsumerWarps + 1);
     }
@@ -688,16 +701,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ++sseq;
           }
           if (t >= 1) {  // weighted values of key tile t - 1
-            const int vs = vseq % kStages;
-            if (!wait_or_abort(&s.pfull, pseq & 1, abort) ||
+            const int vs = vseq % kStages, pb = pseq & 1;
+            if (!wait_or_abort(&s.pfull[pb], (pseq >> 1) & 1, abort) ||
                 !wait_or_abort(&s.vfull[vs], (vseq / kStages) & 1, abort) ||
                 (t == 1 && ocount >= 1 && !wait_or_abort(&s.o_empty, (ocount - 1) & 1, abort))) {
               stop = true;
               break;
             }
             tc_fence_after();
-            issue_pv_mma<D>(tmem + kAttnOCol, smem_addr(s.p), smem_addr(s.v[vs]), t > 1);
-            umma_commit(&s.pempty);
+            issue_pv_mma<D>(tmem + kAttnOCol, tmem + kAttnPCol + pb * 64, smem_addr(s.v[vs]),
+                            t > 1);
+            umma_commit(&s.pempty[pb]);
             umma_commit(&s.vempty[vs]);
             ++pseq;
             ++vseq;
@@ -768,18 +782,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             pk[e >> 1] = pack_bf16x2_rn(p0, p1);
           }
         }
-        if (pseq >= 1 && !wait_or_abort(&s.pempty, (pseq - 1) & 1, abort)) {
+        const int pb = pseq & 1;
+        if (pseq >= 2 && !wait_or_abort(&s.pempty[pb], ((pseq >> 1) - 1) & 1, abort)) {
           stop = true;
           break;
         }
-        uint8_t* pt = s.p;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(pt + sw128_offset(row, cg * 32 + c * 8)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        fence_proxy_async_smem();  // generic writes, read next by the tensor cores
+        tc_fence_after();
+        tmem_st16(lane_base + kAttnPCol + pb * 64 + cg * 16, pk);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.pfull);
+        if (lane == 0) mbar_arrive(&s.pfull[pb]);
         ++pseq;
       }
       if (stop) break;
