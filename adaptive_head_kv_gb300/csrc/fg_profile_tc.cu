@@ -547,6 +547,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -684,37 +697,61 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&s.unit_empty[us]);
         if (!um.valid) break;
         if (!wait_or_abort(&s.a_full[us], (ucount >> 1) & 1, abort)) break;
+        // Issue order follows readiness: a tile's scores go out as soon as
+        // its K tile has landed and the score buffer it reuses has been read
+        // (up to two tiles ahead of the consumers), a tile's P V as soon as
+        // its weights are in tensor memory.  One thread polls both.
         bool stop = false;
-        for (int t = 0; t <= um.nb && !stop; ++t) {
-          if (t < um.nb) {  // scores of key tile t
+        int si = 0, pi = 0, idle = 0;
+        uint64_t t0 = global_timer_ns();
+        while (pi < um.nb) {
+          bool did = false;
+          if (si < um.nb) {  // scores of key tile si
             const int ks = kseq % kStages, sb = sseq & 1;
-            if (!wait_or_abort(&s.kfull[ks], (kseq / kStages) & 1, abort) ||
-                (sseq >= 2 && !wait_or_abort(&s.s_empty[sb], ((sseq >> 1) - 1) & 1, abort))) {
-              stop = true;
-              break;
+            if (mbar_test(&s.kfull[ks], (kseq / kStages) & 1) &&
+                (sseq < 2 || mbar_test(&s.s_empty[sb], ((sseq >> 1) - 1) & 1))) {
+              tc_fence_after();
+              issue_tile_mma<D>(tmem + sb * kBlk, smem_addr(s.q[us]), smem_addr(s.k[ks]));
+              umma_commit(&s.s_full[sb]);
+              umma_commit(&s.kempty[ks]);
+              ++kseq;
+              ++sseq;
+              ++si;
+              did = true;
             }
-            tc_fence_after();
-            issue_tile_mma<D>(tmem + sb * kBlk, smem_addr(s.q[us]), smem_addr(s.k[ks]));
-            umma_commit(&s.s_full[sb]);
-            umma_commit(&s.kempty[ks]);
-            ++kseq;
-            ++sseq;
           }
-          if (t >= 1) {  // weighted values of key tile t - 1
+          if (pi < si) {  // weighted values of key tile pi
             const int vs = vseq % kStages, pb = pseq & 1;
-            if (!wait_or_abort(&s.pfull[pb], (pseq >> 1) & 1, abort) ||
-                !wait_or_abort(&s.vfull[vs], (vseq / kStages) & 1, abort) ||
-                (t == 1 && ocount >= 1 && !wait_or_abort(&s.o_empty, (ocount - 1) & 1, abort))) {
+            if (mbar_test(&s.pfull[pb], (pseq >> 1) & 1) &&
+                mbar_test(&s.vfull[vs], (vseq / kStages) & 1) &&
+                (pi > 0 || ocount == 0 || mbar_test(&s.o_empty, (ocount - 1) & 1))) {
+              tc_fence_after();
+              issue_pv_mma<D>(tmem + kAttnOCol, tmem + kAttnPCol + pb * 64, smem_addr(s.v[vs]),
+                              pi > 0);
+              umma_commit(&s.pempty[pb]);
+              umma_commit(&s.vempty[vs]);
+              ++pseq;
+              ++vseq;
+              ++pi;
+              did = true;
+            }
+          }
+          if (did) {
+            idle = 0;
+            t0 = global_timer_ns();
+            continue;
+          }
+          if (*abort) {
+            stop = true;
+            break;
+          }
+          if (++idle >= 64) {  // bounded like every other wait
+            idle = 0;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              *abort = 1;
               stop = true;
               break;
             }
-            tc_fence_after();
-            issue_pv_mma<D>(tmem + kAttnOCol, tmem + kAttnPCol + pb * 64, smem_addr(s.v[vs]),
-                            t > 1);
-            umma_commit(&s.pempty[pb]);
-            umma_commit(&s.vempty[vs]);
-            ++pseq;
-            ++vseq;
           }
         }
         if (stop) break;
