@@ -154,7 +154,8 @@ __device__ __forceinline__ void lse_tile(uint32_t (&r)[2][32], float sl2, int c0
 }
 
 // Pass 2, one thread's NC x 32 columns (starting at tile column c0) of a key row:
-// adds sum A to cs and the part inside the band to bs.  nl = negated base-2
+// adds sum A to cs and the part inside the band to bs.  Called by all lanes of
+// a warp together.  nl = negated base-2
 // LSEs of the tile's 128 queries (-inf past the prompt end).  Tile columns
 // c < lo precede the key (masked); columns c < band lie in the window.
 template <int NC>
@@ -162,7 +163,8 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
                                          int c0, int lo, int band, float& cs, float& bs) {
   constexpr int kCols = NC * 32;
   const uint64_t s2 = pack2(sl2, sl2);
-  if (lo <= c0 && (band <= c0 || band >= c0 + kCols)) {  // no per-element test
+  // no lane of the warp needs a per-element test: one packed path
+  if (__all_sync(0xffffffffu, lo <= c0 && (band <= c0 || band >= c0 + kCols))) {
     uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int c = 0; c < NC; ++c)
@@ -186,19 +188,38 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
     if (band >= c0 + kCols) bs += t;
     return;
   }
-  float ta[4] = {0.f, 0.f, 0.f, 0.f}, ba[4] = {0.f, 0.f, 0.f, 0.f};
+  // Some lane of the warp needs per-element tests (its causal diagonal or
+  // band edge falls in these columns).  The decision is made for the whole
+  // warp, so its lanes never split between two paths: every lane runs the
+  // packed arithmetic, the causal test only when some lane needs it, and the
+  // band split by a per-element select.
+  const bool diag = __any_sync(0xffffffffu, lo > c0);
+  uint64_t at = 0, ab = 0;
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < 32; e += 4) {
       const int col = c0 + c * 32 + e;
-      float p = ex2(fmaf(f(r[c][e]), sl2, nl[col]));
-      p = col < lo ? 0.f : p;
-      ta[e & 3] += p;
-      ba[e & 3] += col < band ? p : 0.f;
+      const float4 L = *reinterpret_cast<const float4*>(nl + col);
+      float x0, x1, x2, x3;
+      unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
+      unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
+      float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+      if (diag) {
+        p0 = col < lo ? 0.f : p0;
+        p1 = col + 1 < lo ? 0.f : p1;
+        p2 = col + 2 < lo ? 0.f : p2;
+        p3 = col + 3 < lo ? 0.f : p3;
+      }
+      at = add2(at, add2(pack2(p0, p1), pack2(p2, p3)));
+      ab = add2(ab, add2(pack2(col < band ? p0 : 0.f, col + 1 < band ? p1 : 0.f),
+                         pack2(col + 2 < band ? p2 : 0.f, col + 3 < band ? p3 : 0.f)));
     }
-  cs += (ta[0] + ta[1]) + (ta[2] + ta[3]);
-  bs += (ba[0] + ba[1]) + (ba[2] + ba[3]);
+  float t0, t1, b0, b1;
+  unpack2(at, t0, t1);
+  unpack2(ab, b0, b1);
+  cs += t0 + t1;
+  bs += b0 + b1;
 }
 
 // PASS 1: nlse2[g, i] = -log2 sum_j 2^(s' q_i.k_j) (row stride ld); rows past
