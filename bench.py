@@ -290,8 +290,10 @@ def run_ours(args, cfg, rank, world):
     prof_flops = 2.0 * n * (n + 1) * d * G
     kept_rows = int((ckeep != 0).sum())
     comp_bytes = kept_rows * d * 2 * eb * 2 + G * n + Gkv * 40
-    pmap = run_policy_map(args, s, Q, K, V, ids, stream)
-    pattn = run_prompt_attention(args, s, cfg, Q, K, V, ids, stream)
+    pmap = pattn = None
+    if not args.no_extras:
+        pmap = run_policy_map(args, s, Q, K, V, ids, stream)
+        pattn = run_prompt_attention(args, s, cfg, Q, K, V, ids, stream)
     return dict(cfg=cfg, prof_ms=prof_ms, comp_ms=comp_ms, decode_ms=decode_ms, step_ms=step_ms,
                 total_ms=total_ms, dec_ms=dec_ms, dec_bytes=float(dec_bytes_t.mean()),
                 dec_gbs=dec_gbs, prof_flops=prof_flops, comp_bytes=comp_bytes,
@@ -499,6 +501,9 @@ def main():
                     help="key/value heads per layer (grouped-query attention); 0 = H")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every decode call from the host instead of one CUDA graph")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side measurements (saved policy map, prompt attention "
+                         "output), e.g. for DRAM captures of the main step's kernels")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (smaller cases for profiler captures)")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
@@ -569,8 +574,9 @@ def main():
         "phases_ms": {"profile": r["prof_ms"], "compact_plan": r["comp_ms"],
                       "decode_all_steps": r["decode_ms"], "decode_per_step": dec_launch_ms},
         "kept_fraction": r["kept_frac"],
-        "saved_policy_map": dict(r["policy_map"], prompt_tok_s=world * cfg.B * cfg.n / (
-            (r["policy_map"]["profile_ms"] + r["policy_map"]["compact_plan_ms"]) * 1e-3)),
+        "saved_policy_map": None if r["policy_map"] is None else dict(
+            r["policy_map"], prompt_tok_s=world * cfg.B * cfg.n / (
+                (r["policy_map"]["profile_ms"] + r["policy_map"]["compact_plan_ms"]) * 1e-3)),
         "prompt_attention_output": r["prompt_attention"],
         "roofline": dominant, "roofline_other": other,
         "clocks": r["clocks"],
