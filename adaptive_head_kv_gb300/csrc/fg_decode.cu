@@ -601,19 +601,35 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
   const fg_head_desc hd = a.desc[c];
   const size_t w0 = (size_t)hd.work_off;
   const int nw = hd.n_work;
-  float M = FG_NEG_INF;
-#pragma unroll 4
-  for (int i = 0; i < nw; ++i) M = fmaxf(M, a.part_ml[2 * ((w0 + i) * R + q)]);
-  float L = 0.f, acc = 0.f;
-  if (M != FG_NEG_INF) {
-#pragma unroll 4
-    for (int i = 0; i < nw; ++i) {
-      const size_t slot = (w0 + i) * R + q;
-      const float mi = a.part_ml[2 * slot];
-      const float wgt = mi == FG_NEG_INF ? 0.f : exp2f(mi - M);
-      L = fmaf(wgt, a.part_ml[2 * slot + 1], L);
-      acc = fmaf(wgt, a.part_acc[slot * D + t], acc);
+  // items in chunks of 8: every load of a chunk is issued before any is used
+  // (one memory round trip per chunk), then merged into the running
+  // (M, L, acc) with a log-sum-exp rescale
+  float M = FG_NEG_INF, L = 0.f, acc = 0.f;
+  for (int i0 = 0; i0 < nw; i0 += 8) {
+    float m[8], l[8], x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool ok = i0 + j < nw;
+      const size_t slot = (w0 + i0 + j) * R + q;
+      m[j] = ok ? a.part_ml[2 * slot] : FG_NEG_INF;
+      l[j] = ok ? a.part_ml[2 * slot + 1] : 0.f;
+      x[j] = ok ? a.part_acc[slot * D + t] : 0.f;
     }
+    float mc = m[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) mc = fmaxf(mc, m[j]);
+    const float Mn = fmaxf(M, mc);
+    if (Mn == FG_NEG_INF) continue;
+    const float f = M == FG_NEG_INF ? 0.f : exp2f(M - Mn);
+    L *= f;
+    acc *= f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float wgt = m[j] == FG_NEG_INF ? 0.f : exp2f(m[j] - Mn);
+      L = fmaf(wgt, l[j], L);
+      acc = fmaf(wgt, x[j], acc);
+    }
+    M = Mn;
   }
   store_out((T*)a.out + (size_t)g * D + t, L > 0.f ? acc / L : 0.f);
   if (t == 0 && q == 0) {  // one member advances the shared cache
