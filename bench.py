@@ -555,7 +555,15 @@ def main():
     prof_roof = {"kernel": "fastgen_profile (token classes, both passes, select)",
                  "bound": "tensor", "achieved": prof_ach, "peak": pk["bf16"], "unit": "TFLOP/s",
                  "frac": prof_ach / pk["bf16"], "traffic": load_traffic("profile", cfg.name),
-                 "peak_source": pk["src"], "algorithmic_flops_per_launch": r["prof_flops"]}
+                 "peak_source": pk["src"], "algorithmic_flops_per_launch": r["prof_flops"],
+                 # the flops of one causal Q K^T per head over the same time (the
+                 # column sums need the final row LSEs, hence the second pass)
+                 "one_pass_equivalent_tflops": prof_ach / 2}
+    comp_gbs = r["comp_bytes"] / (r["comp_ms"] * 1e-3) / 1e9
+    comp_roof = {"kernel": "fastgen_compact_plan + fastgen_compact (plan, gather)", "bound": "hbm",
+                 "achieved": comp_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                 "frac": comp_gbs / pk["hbm"], "peak_source": pk["src"],
+                 "algorithmic_bytes_per_call": r["comp_bytes"]}
     dec_total = r["decode_ms"]
     dominant, other = (dec_roof, prof_roof) if dec_total >= r["prof_ms"] else (prof_roof, dec_roof)
     e = r["e2e"]
@@ -579,7 +587,7 @@ def main():
             r["policy_map"], prompt_tok_s=world * cfg.B * cfg.n / (
                 (r["policy_map"]["profile_ms"] + r["policy_map"]["compact_plan_ms"]) * 1e-3)),
         "prompt_attention_output": r["prompt_attention"],
-        "roofline": dominant, "roofline_other": other,
+        "roofline": dominant, "roofline_other": other, "roofline_compaction": comp_roof,
         "clocks": r["clocks"],
         "e2e": {"value": world * cfg.B * cfg.n / (e["prefill_ms"] * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
