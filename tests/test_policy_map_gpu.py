@@ -153,3 +153,77 @@ def test_out_of_range_saved_value_is_reported():
     assert fg.fastgen_read_error(s.dev_err) == fg.FG_EINVAL
     keep = s.keep.cpu().numpy()
     assert np.all(keep[1] == fg.FG_KEEP_STATIC)  # read as the full cache
+
+
+def test_saved_map_with_grouped_keys():
+    """A hand-set map on grouped keys (two query heads per key/value head):
+    each query head's keep codes, and every member's decode output over the
+    group's union cache (largest member policy), against the oracle."""
+    from oracle import fastgen_oracle as O
+    from parity_util import dec_atol, kv_rows
+    from synth import make_workload, punct_ids, special_ids
+
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=4, Hkv=2, n=300, steps=10)
+    pmap = np.array([0, 4, 1, 2, 3, 0, 2, 1], dtype=np.int8)  # G = 8: every pairing kind
+    w = make_workload(cfg, 5)
+    n, dev = cfg.n, torch.device("cuda")
+    p, s = _session(cfg, cfg.steps)
+    sel = kv_rows(cfg)
+    Q = w["Q"][:, :n].contiguous().to(dev)
+    K = w["K"][sel, :n].contiguous().to(dev)
+    V = w["V"][sel, :n].contiguous().to(dev)
+    ids = torch.from_numpy(w["ids"]).to(dev)
+    s.prefill_with_policy(Q, K, V, ids[:, :n].contiguous(), pmap)
+    Qd = w["Q"][:, n:].transpose(0, 1).contiguous().to(dev)
+    Kd = w["K"][sel, n:].transpose(0, 1).contiguous().to(dev)
+    Vd = w["V"][sel, n:].transpose(0, 1).contiguous().to(dev)
+    idd = ids[:, n:].transpose(0, 1).contiguous()
+    outs = torch.empty(cfg.steps, s.G, cfg.d, dtype=s.tdtype, device=dev)
+    for st in range(cfg.steps):
+        s.decode(Qd[st], Kd[st], Vd[st], idd[st], n + st, out=outs[st])
+    torch.cuda.synchronize()
+    assert fg.fastgen_read_error(s.dev_err) == fg.FG_OK
+    assert s.check_guards() == 0
+    keep = s.keep.cpu().numpy()
+    outs = outs.float().cpu().numpy().astype(np.float64)
+    r = cfg.H // cfg.kv_heads
+    ids0 = w["ids"][0]
+    for c, g0 in enumerate(sel):
+        members = list(range(g0, g0 + r))
+        Qs = [w["Q"][g].double().numpy() for g in members]
+        Ka, Va = w["K"][g0].double().numpy(), w["V"][g0].double().numpy()
+        keeps = []
+        for g, Qa in zip(members, Qs):
+            ora = O.profile_with_policy(int(pmap[g]), Qa[:n], Ka[:n], ids0, special_ids(),
+                                        punct_ids(), cfg.r_l, cfg.r_f)
+            if ora["colsum"] is not None and _topk_tied(ora["colsum"], O.ratio_count(cfg.r_f, n)):
+                # several top-k sets are correct: the GPU's must be one of them
+                k = O.ratio_count(cfg.r_f, n)
+                spec, punc = O.token_sets(ids0[:n], special_ids(), punct_ids())
+                chosen = (keep[g] == O.KEEP_STATIC) & ~(spec | punc)
+                others = ~(spec | punc) & ~chosen
+                ck = np.sort(ora["colsum"])[::-1][k - 1]
+                tol = 2e-5 * max(1.0, ck)
+                assert np.all(ora["colsum"][chosen] >= ck - tol), g
+                assert np.all(ora["colsum"][others] <= ck + tol), g
+                # (the kept count may differ: tied keys inside the window overlap it)
+                assert ((keep[g] == O.KEEP_STATIC) & ~(spec | punc)).sum() <= k, g
+                keeps.append(keep[g])
+                continue
+            assert np.array_equal(keep[g], ora["keep"]), g
+            keeps.append(ora["keep"])
+        gkeep = O.union_keep(keeps)
+        gpol = int(max(pmap[g] for g in members))
+        out, _ = O.decode_group(gpol, gkeep, n, O.ratio_count(cfg.r_l, n), ids0, Qs, Ka, Va,
+                                special_ids(), punct_ids(), cfg.steps)
+        for mi, g in enumerate(members):
+            err = np.abs(outs[:, g] - out[mi]).max()
+            assert err <= dec_atol(cfg.dtype), (c, g, err)
+
+
+def _topk_tied(colsum, k):
+    c = np.sort(colsum)[::-1]
+    return 0 < k < c.shape[0] and c[k - 1] - c[k] <= 1e-5 * max(1.0, c[k - 1])
+
