@@ -572,9 +572,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded generator, planted head types; no weights or datasets)",
-        "config": {"workload": f"{cfg.name}: B={cfg.B} L={cfg.L} H={cfg.H} Hkv={cfg.kv_heads} "
-                               f"d={cfg.d} n={cfg.n} decode_steps={cfg.steps} T={cfg.T} "
-                               f"r_l={cfg.r_l} r_f={cfg.r_f}",
+        "config": {"workload": workload_name(cfg),
                    "G": cfg.G, "parallelism": f"replicas x{world}",
                    "l2": "inputs and caches larger than L2 (no flush)",
                    "step": "profile + plan + compact + all decode steps",
@@ -610,6 +608,12 @@ def fg_launches(call):
     return LAUNCHES[call]
 
 
+def workload_name(cfg):
+    """The workload as both arms name it in `config.workload`."""
+    return (f"{cfg.name}: B={cfg.B} L={cfg.L} H={cfg.H} Hkv={cfg.kv_heads} d={cfg.d} n={cfg.n} "
+            f"decode_steps={cfg.steps} T={cfg.T} r_l={cfg.r_l} r_f={cfg.r_f}")
+
+
 def run_reference(args, cfg, world):
     """The oracle timed as it stands on the host cores, on bounded samples of
     the same workload, reported in the same metric (extrapolated linearly in
@@ -635,7 +639,7 @@ def run_reference(args, cfg, world):
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall_ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded generator)",
-           "config": {"workload": f"{cfg.name}", "G": cfg.G,
+           "config": {"workload": workload_name(cfg), "G": cfg.G,
                       "step": f"{heads_per_step} sampled heads (profile+compact+{cfg.steps} "
                               f"decode steps each); value extrapolated to all {cfg.G} heads"},
            "extrapolated_ms_per_full_step": (t_pc + t_dec) * scale / max(args.steps, 1) * 1e3,
