@@ -109,8 +109,15 @@ __global__ void worklist_kernel(const fg_head_desc* __restrict__ desc, int G,
   for (int i = 0; i < hd.n_work; ++i) work[hd.work_off + i] = make_int2(g, i);
 }
 
-// One CTA per head: scan the keep codes in tiles of 256 positions, then copy
-// the tile's kept rows with 16-byte vectors, one row per LPR lanes.
+// One CTA per (cache, chunk of kCompactChunk prompt positions): the CTA first
+// counts the never-evicted rows before its chunk (their count is the first
+// row it fills), then scans its positions in tiles of 256 and copies each
+// tile's kept rows with 16-byte vectors, one row per LPR lanes.  A window
+// position's ring slot (position mod w) is written by the CTA that owns the
+// position: its position if the row lives in the window, else the empty
+// marker; chunk 0 also marks the segment's reserve rows empty.
+constexpr int kCompactChunk = 512;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
     const T* __restrict__ K, const T* __restrict__ V, const uint8_t* __restrict__ keep,
@@ -121,24 +128,31 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
   __shared__ int scr[33];
   __shared__ int src_pos[kCompactThreads];
   __shared__ long long dst_row[kCompactThreads];
-  const int g = blockIdx.x;  // key/value head
+  const int g = blockIdx.y;  // key/value head
+  const int j0 = blockIdx.x * kCompactChunk, j1 = min(j0 + kCompactChunk, n);
   const fg_head_desc hd = desc[g];
   const int Hkv = H / R;
   const size_t g0 = (size_t)(g / Hkv) * H + (size_t)(g % Hkv) * R;  // its first query head
-  // empty markers: reserve rows of the static segment and every ring slot
-  for (int r = hd.n_static + threadIdx.x; r < hd.static_cap; r += blockDim.x)
-    posp[hd.off + r] = -1;
-  for (int r = threadIdx.x; r < hd.w; r += blockDim.x) posp[hd.win_off + r] = -1;
-  __syncthreads();
-  int static_seen = 0;
-  for (int base = 0; base < n; base += blockDim.x) {
+  if (blockIdx.x == 0)  // empty markers on the reserve rows of the segment
+    for (int r = hd.n_static + threadIdx.x; r < hd.static_cap; r += blockDim.x)
+      posp[hd.off + r] = -1;
+  int before = 0;  // never-evicted rows at positions < j0
+  for (int j = threadIdx.x; j < j0; j += blockDim.x)
+    before += union_code(keep, g0, R, n, j) == FG_KEEP_STATIC ? 1 : 0;
+  int static_seen;
+  block_exclusive_scan(before, scr, &static_seen);
+  const T* Kg = K + (size_t)g * n * D;
+  const T* Vg = V + (size_t)g * n * D;
+  for (int base = j0; base < j1; base += blockDim.x) {
     const int j = base + threadIdx.x;
-    const int code = j < n ? union_code(keep, g0, R, n, j) : FG_KEEP_DROP;
+    const int code = j < j1 ? union_code(keep, g0, R, n, j) : FG_KEEP_DROP;
     const int is_static = code == FG_KEEP_STATIC;
     const int is_kept = code != FG_KEEP_DROP;
     int st_total, kept_total;
     const int st_rank = static_seen + block_exclusive_scan(is_static, scr, &st_total);
     const int slot = block_exclusive_scan(is_kept, scr, &kept_total);
+    if (hd.w > 0 && j < j1 && j >= n - hd.w && code != FG_KEEP_WINDOW)
+      posp[hd.win_off + j % hd.w] = -1;  // a window position kept elsewhere (or not at all)
     if (is_kept) {
       long long dst;
       if (is_static) dst = hd.off + st_rank;
@@ -149,8 +163,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
     }
     static_seen += st_total;
     __syncthreads();
-    const T* Kg = K + (size_t)g * n * D;
-    const T* Vg = V + (size_t)g * n * D;
+#pragma unroll 4
     for (int v = threadIdx.x; v < kept_total * LPR; v += blockDim.x) {
       const int r = v / LPR, c = (v % LPR) * E;
       const size_t s = (size_t)src_pos[r] * D + c;
@@ -168,8 +181,9 @@ template <typename T, int D>
 cudaError_t run_compact(const ProfileDims& pd, const void* K, const void* V, const uint8_t* keep,
                         const fg_head_desc* desc, void* Kp, void* Vp, int32_t* posp,
                         cudaStream_t s) {
-  compact_kernel<T, D><<<pd.Gkv, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
-                                                          pd.n, pd.H, pd.R, (T*)Kp, (T*)Vp, posp);
+  const dim3 grid(cdiv(pd.n, kCompactChunk), pd.Gkv);
+  compact_kernel<T, D><<<grid, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
+                                                        pd.n, pd.H, pd.R, (T*)Kp, (T*)Vp, posp);
   return cudaGetLastError();
 }
 
