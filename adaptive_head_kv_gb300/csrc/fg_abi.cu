@@ -246,6 +246,19 @@ fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, cons
   return cuda_status(e);
 }
 
+fg_status fastgen_plan_compact(const fg_params* p, const int8_t* policy, const uint8_t* keep,
+                               int32_t max_new_tokens, void* plan, size_t plan_bytes,
+                               const void* K, const void* V, void* K_pool, void* V_pool,
+                               int32_t* pos_pool, int64_t pool_rows, fg_plan_info* info,
+                               void* stream) {
+  if (!K || !V || !K_pool || !V_pool || !pos_pool) return FG_EINVAL;
+  fg_status st = fastgen_compact_plan(p, policy, keep, max_new_tokens, plan, plan_bytes, info,
+                                      stream);
+  if (st != FG_OK) return st;
+  if (pool_rows < info->pool_rows) return FG_EWORKSPACE;  // info tells the caller what to allocate
+  return fastgen_compact(p, K, V, keep, plan, info, K_pool, V_pool, pos_pool, pool_rows, stream);
+}
+
 size_t fastgen_decode_workspace_bytes(const fg_params* p, const fg_plan_info* info) {
   if (check_params(p) != FG_OK || !info || info->n_work < 0) return 0;
   const size_t nw = (size_t)info->n_work * group_size(p);  // one partial per item and query

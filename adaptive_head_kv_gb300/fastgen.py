@@ -79,6 +79,9 @@ _SIGS = {
                                             ctypes.POINTER(PlanInfo), _P]),
     "fastgen_compact": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P,
                                        ctypes.POINTER(PlanInfo), _P, _P, _P, _I64, _P]),
+    "fastgen_plan_compact": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, ctypes.c_int32, _P,
+                                            _SZ, _P, _P, _P, _P, _P, _I64,
+                                            ctypes.POINTER(PlanInfo), _P]),
     "fastgen_decode_workspace_bytes": (_SZ, [ctypes.POINTER(Params), ctypes.POINTER(PlanInfo)]),
     "fastgen_decode_attn": (ctypes.c_int, [ctypes.POINTER(Params), _P, ctypes.POINTER(PlanInfo),
                                            _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
@@ -195,6 +198,21 @@ def fastgen_compact(params, K, V, keep, plan, info, K_pool, V_pool, pos_pool, st
     _check(lib().fastgen_compact(ctypes.byref(params), _ptr(K), _ptr(V), _ptr(keep), _ptr(plan),
                                  ctypes.byref(info), _ptr(K_pool), _ptr(V_pool), _ptr(pos_pool),
                                  int(pos_pool.numel()), _stream(stream)), "fastgen_compact")
+
+
+def fastgen_plan_compact(params, policy, keep, max_new_tokens, plan, K, V, K_pool, V_pool,
+                         pos_pool, stream=None):
+    """Plan and gather in one call.  Returns (done, info): done is False when
+    the pools are smaller than info.pool_rows (nothing was gathered)."""
+    info = PlanInfo()
+    st = lib().fastgen_plan_compact(
+        ctypes.byref(params), _ptr(policy), _ptr(keep), max_new_tokens, _ptr(plan),
+        plan.numel() * plan.element_size(), _ptr(K), _ptr(V), _ptr(K_pool), _ptr(V_pool),
+        _ptr(pos_pool), int(pos_pool.numel()), ctypes.byref(info), _stream(stream))
+    if st == FG_EWORKSPACE and info.pool_rows > pos_pool.numel():
+        return False, info
+    _check(st, "fastgen_plan_compact")
+    return True, info
 
 
 def fastgen_decode_workspace_bytes(params: Params, info: PlanInfo) -> int:

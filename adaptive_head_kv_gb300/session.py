@@ -86,19 +86,30 @@ class FastGenSession:
         self.compact(K, V)
 
     def compact(self, K, V):
-        self.info = fg.fastgen_compact_plan(self.p, self.policy, self.keep, self.max_new,
-                                            self.plan, self.stream)
+        if self.pos_pool is not None:  # pools from an earlier prompt: plan and gather in one call
+            done, self.info = fg.fastgen_plan_compact(self.p, self.policy, self.keep, self.max_new,
+                                                      self.plan, K, V, self.K_pool, self.V_pool,
+                                                      self.pos_pool, self.stream)
+            self._size_decode_workspace()
+            if done:
+                return
+        else:
+            self.info = fg.fastgen_compact_plan(self.p, self.policy, self.keep, self.max_new,
+                                                self.plan, self.stream)
         rows = int(self.info.pool_rows)
         if self.pos_pool is None or self.pos_pool.numel() < rows:
             d = self.p.d
             self.K_pool = self._empty((rows, d), self.tdtype)
             self.V_pool = self._empty((rows, d), self.tdtype)
             self.pos_pool = self._empty((rows,), torch.int32)
+        self._size_decode_workspace()
+        fg.fastgen_compact(self.p, K, V, self.keep, self.plan, self.info, self.K_pool,
+                           self.V_pool, self.pos_pool, self.stream)
+
+    def _size_decode_workspace(self):
         need = fg.fastgen_decode_workspace_bytes(self.p, self.info)
         if self.dws is None or self.dws.numel() < need:
             self.dws = self._empty((max(need, 256),), torch.uint8)
-        fg.fastgen_compact(self.p, K, V, self.keep, self.plan, self.info, self.K_pool,
-                           self.V_pool, self.pos_pool, self.stream)
 
     def prefill(self, Q, K, V, token_ids):
         self.profile(Q, K, token_ids)

@@ -246,6 +246,21 @@ fg_status fastgen_compact(const fg_params* p, const void* K, const void* V, cons
                           void* V_pool, int32_t* pos_pool, int64_t pool_rows, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Compaction, both steps in one call: fastgen_compact_plan, then, if the
+ * caller's pools hold info->pool_rows rows, fastgen_compact at once (no
+ * return to the caller between the plan's host read-back and the gather
+ * launch).  Arguments as for those two calls; `info` is always filled when
+ * the plan succeeded.  Returns FG_EWORKSPACE without launching the gather when
+ * pool_rows < info->pool_rows (the caller allocates that many rows and calls
+ * fastgen_compact).  Synchronous like fastgen_compact_plan.
+ * ------------------------------------------------------------------------ */
+fg_status fastgen_plan_compact(const fg_params* p, const int8_t* policy, const uint8_t* keep,
+                               int32_t max_new_tokens, void* plan, size_t plan_bytes,
+                               const void* K, const void* V, void* K_pool, void* V_pool,
+                               int32_t* pos_pool, int64_t pool_rows, fg_plan_info* info,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
  * Generation step for every head (Method: head-specific caches, appends,
  * policy reused from the prompt).
  *

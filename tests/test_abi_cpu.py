@@ -147,6 +147,19 @@ def test_policy_map_json_roundtrip(tmp_path):
         save_policy_map(path, p, pol[:5])
 
 
+def test_plan_compact_in_one_call_rejects_on_host():
+    L = fg.lib()
+    p = P()
+    info = fg.PlanInfo()
+    need = fg.fastgen_plan_bytes(p, 4)
+    call = lambda K=FAKE, plan=FAKE, nbytes=need: L.fastgen_plan_compact(
+        ctypes.byref(p), FAKE, FAKE, 4, plan, nbytes, K, FAKE, FAKE, FAKE, FAKE, 1000,
+        ctypes.byref(info), None)
+    assert call(K=None) == fg.FG_EINVAL
+    assert call(nbytes=need - 1) == fg.FG_EWORKSPACE
+    assert call(plan=FAKE + 32) == fg.FG_EINVAL
+
+
 def test_plan_compact_decode_reject_on_host():
     L = fg.lib()
     p = P()
