@@ -37,19 +37,6 @@ __global__ void token_class_kernel(const int32_t* __restrict__ ids, int count,
   cls[i] = (uint8_t)((id_in(id, special, ns) ? 1 : 0) | (id_in(id, punct, np) ? 2 : 0));
 }
 
-template <typename V>
-__device__ __forceinline__ V block_sum(V x, V* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  V t = V(0);
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
-  return t;
-}
-
 // Membership bits kept in `keep` between the two sweeps: 1 = K^0,
 // 2 = K^1, 4 = K^2, 8 = inside the last-w window.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
@@ -62,8 +49,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   __shared__ unsigned hist[256];
   __shared__ int s_bin, s_krem, s_eq;
   __shared__ int scan_scratch[33];
-  __shared__ double dred[32];
-  __shared__ int ired[32];
+  __shared__ double sred_a[kSelThreads / 32][4];
+  __shared__ int sred_c[kSelThreads / 32][4];
   __shared__ int s_policy;
 
   griddep_wait();
@@ -174,10 +161,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     if (s2 || win) ++c3;
     kp[j] = (uint8_t)((s0 ? 1 : 0) | (s1 ? 2 : 0) | (s2 ? 4 : 0) | (win ? 8 : 0));
   }
-  a0 = block_sum(a0, dred); a1 = block_sum(a1, dred);
-  a2 = block_sum(a2, dred); a3 = block_sum(a3, dred);
-  c0 = block_sum(c0, ired); c1 = block_sum(c1, ired);
-  c2 = block_sum(c2, ired); c3 = block_sum(c3, ired);
+  // the eight sums at once: warp shuffles, then one pass over the warps
+  {
+    double av[4] = {a0, a1, a2, a3};
+    int cv[4] = {c0, c1, c2, c3};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        av[q] += __shfl_xor_sync(0xffffffffu, av[q], o);
+        cv[q] += __shfl_xor_sync(0xffffffffu, cv[q], o);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sred_a[warp][q] = av[q];
+        sred_c[warp][q] = cv[q];
+      }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      a0 = a1 = a2 = a3 = 0.0;
+      c0 = c1 = c2 = c3 = 0;
+      for (int w = 0; w < kSelThreads / 32; ++w) {
+        a0 += sred_a[w][0]; a1 += sred_a[w][1]; a2 += sred_a[w][2]; a3 += sred_a[w][3];
+        c0 += sred_c[w][0]; c1 += sred_c[w][1]; c2 += sred_c[w][2]; c3 += sred_c[w][3];
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     const double inv = 1.0 / (double)n;
     const double m[5] = {a0 * inv, a1 * inv, a2 * inv, a3 * inv, 1.0};
