@@ -227,3 +227,35 @@ def _topk_tied(colsum, k):
     c = np.sort(colsum)[::-1]
     return 0 < k < c.shape[0] and c[k - 1] - c[k] <= 1e-5 * max(1.0, c[k - 1])
 
+
+
+def test_pools_grow_between_prompts():
+    """One session, two prompts: the second needs larger pools than the
+    first left (all full caches after all special-only ones), so the one-call
+    plan + gather reports the size and the session grows the pools and
+    gathers again; the second prompt's decode matches the oracle."""
+    from synth import make_workload
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=1, H=4, n=200, steps=6)
+    p, s = _session(cfg, cfg.steps)
+    w0 = make_workload(cfg, 6)
+    Q, K, V, ids = _device_inputs(w0, cfg.n)
+    s.prefill_with_policy(Q, K, V, ids[:, :cfg.n].contiguous(), np.zeros(cfg.G, np.int8))
+    small = s.pos_pool.numel()
+    full = np.full(cfg.G, 4, dtype=np.int8)
+    w = make_workload(cfg, 7)
+    Q, K, V, ids = _device_inputs(w, cfg.n)
+    s.prefill_with_policy(Q, K, V, ids[:, :cfg.n].contiguous(), full)
+    assert s.pos_pool.numel() > small
+    dev = Q.device
+    n = cfg.n
+    Qd = w["Q"][:, n:].transpose(0, 1).contiguous().to(dev)
+    Kd = w["K"][:, n:].transpose(0, 1).contiguous().to(dev)
+    Vd = w["V"][:, n:].transpose(0, 1).contiguous().to(dev)
+    idd = ids[:, n:].transpose(0, 1).contiguous()
+    o = torch.empty(cfg.steps, s.G, cfg.d, dtype=s.tdtype, device=dev)
+    for st in range(cfg.steps):
+        s.decode(Qd[st], Kd[st], Vd[st], idd[st], n + st, out=o[st])
+    torch.cuda.synchronize()
+    rep = _compare(cfg, full, w, s, o.float().cpu().numpy().astype(np.float64))
+    assert rep["decode"] == cfg.G, rep
