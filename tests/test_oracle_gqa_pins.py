@@ -72,3 +72,41 @@ def test_union_contains_every_member_cache():
         assert np.all((keep != O.DROP) >= (m["keep"] != O.DROP))
         assert np.all((keep == O.KEEP_STATIC) >= (m["keep"] == O.KEEP_STATIC))
     assert pol == max(m["policy"] for m in members)
+
+
+def test_planted_mistakes_fail_a_pin(monkeypatch):
+    """Plausible mistakes in the grouped extension, one at a time: each must
+    fail one of the pins above."""
+    pins = (test_group_of_one_is_the_head_path, test_union_codes,
+            test_group_rule_matches_window_golden, test_union_contains_every_member_cache)
+    real_union, real_profile, real_attend = O.union_keep, O.profile_group, O.attend
+
+    def window_beats_static(keeps):
+        keeps = np.asarray(keeps)
+        window = (keeps == O.KEEP_WINDOW).any(axis=0)
+        static = (keeps == O.KEEP_STATIC).any(axis=0)
+        return np.where(window, O.KEEP_WINDOW, np.where(static, O.KEEP_STATIC, O.DROP)).astype(
+            np.uint8)
+
+    def smallest_policy(Qs, K, ids, sp, pu, T, r_l, r_f, scale=None):
+        members, keep, _ = real_profile(Qs, K, ids, sp, pu, T, r_l, r_f, scale)
+        return members, keep, min(m["policy"] for m in members)
+
+    def intersection(keeps):
+        keeps = np.asarray(keeps)
+        return np.where((keeps != O.DROP).all(axis=0), real_union(keeps), O.DROP).astype(np.uint8)
+
+    for name, attr, bad in (("window beats static", "union_keep", window_beats_static),
+                            ("smallest member policy", "profile_group", smallest_policy),
+                            ("intersection of caches", "union_keep", intersection)):
+        monkeypatch.setattr(O, attr, bad)
+        failed = 0
+        for pin in pins:
+            try:
+                pin()
+            except AssertionError:
+                failed += 1
+        monkeypatch.setattr(O, attr, {"union_keep": real_union,
+                                      "profile_group": real_profile}[attr])
+        assert failed >= 1, name
+    assert O.attend is real_attend
