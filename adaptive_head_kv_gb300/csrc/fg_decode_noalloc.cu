@@ -9,13 +9,20 @@
 // outputs and caches; only the decode scratch (the split-K partial results)
 // moves into a fixed array inside this library.
 //
-// The array is a file-scope __device__ variable: every GPU that loads the
-// library holds FASTGEN_NOALLOC_SCRATCH_BYTES of it until the process exits.
-// Host code cannot use its name as a device address, so the address is looked
-// up once per device with cudaGetSymbolAddress (with that device current) and
-// cached; the first call on a device does this lookup.  Every call shares the
-// array: calls that overlap on the GPU race.  Each call writes every scratch
-// entry it reads, so nothing needs clearing between calls.
+// The array is a file-scope __device__ variable of this file's own CUDA
+// module.  CUDA sets it aside on a device when it loads that module there:
+// under the default lazy module loading, that happens at the first address
+// look-up below (the first call of the entry point on that device); with
+// CUDA_MODULE_LOADING=EAGER, when the device's context is created.  From then
+// on the device holds FASTGEN_NOALLOC_SCRATCH_BYTES until the process exits,
+// so callers make their first call at set-up, before their own pool takes the
+// free memory and before any stream capture.  Host code cannot use the
+// array's name as a device address, so the address is looked up once per
+// device with cudaGetSymbolAddress (with that device current) and cached for
+// the life of the process (the device's primary context is assumed to live
+// that long).  Every call shares the array: calls that overlap on the GPU
+// race.  Each call writes every scratch entry it reads, so nothing needs
+// clearing between calls.
 #include <mutex>
 
 #include "fg_common.cuh"

@@ -302,19 +302,32 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
  * implicit synchronisation.  This variant takes the same arguments as
  * fastgen_decode_attn minus `workspace`/`workspace_bytes` and allocates
  * nothing: its scratch (the split-K partial results) is a fixed array of
- * FASTGEN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
- * the library holds until the process exits.
- *   - The first call on each device looks up that array's device address
- *     (cudaGetSymbolAddress, with the device current) and caches it; make
- *     that first call before any stream capture.
+ * FASTGEN_NOALLOC_SCRATCH_BYTES inside the library.
+ *   - When the array is set aside: the array lives in its own CUDA module of
+ *     the library, which CUDA loads on a device the first time this entry
+ *     point looks the array up there.  Under CUDA's default lazy module
+ *     loading that is the first call of this entry point on the device (with
+ *     CUDA_MODULE_LOADING=EAGER it is the creation of the device's context);
+ *     from then on the device holds the array until the process exits.  So
+ *     make the first call at set-up: before the caller's own pool takes the
+ *     device's free memory, and before any stream capture.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it for the
+ *     life of the process: the cache assumes the device's primary context is
+ *     never destroyed (no cudaDeviceReset between calls).
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and produce wrong results, so issue
  *     them in order on one stream.  Nothing in the array has to start at
  *     zero: a call writes every entry it later reads.
- *   - Returns FG_EWORKSPACE when the plan needs more scratch than the array
- *     holds, i.e. fastgen_decode_workspace_bytes(p, info) >
- *     FASTGEN_NOALLOC_SCRATCH_BYTES (about 16,000 decode work items at
- *     d = 128); other errors as fastgen_decode_attn.
+ *   - Size limit: the plan fits when fastgen_decode_workspace_bytes(p, info)
+ *     <= FASTGEN_NOALLOC_SCRATCH_BYTES, i.e. roughly
+ *     info->n_work * (H / Hkv) * (d + 2) * 4 bytes <= 8 MiB: about 16,000
+ *     work items at d = 128 without groups, 8,000 with groups of 2, 2,000
+ *     with groups of 8 (one work item covers up to info->rows_per_work = 256
+ *     rows of one cache).  The 7B attention shape (1024 heads, 2048-token
+ *     prompt, 256 new tokens: about 5,600 items) fits; the 13B, 65B and
+ *     long-prompt shapes do not.  Larger plans return FG_EWORKSPACE before
+ *     anything is launched; other errors as fastgen_decode_attn.
  * ------------------------------------------------------------------------ */
 #define FASTGEN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 

@@ -39,3 +39,14 @@ def test_group_caches_union():
     pol, k = bench.group_caches(cfg, policy, keep)
     assert list(pol) == [3, 2]
     assert k.tolist() == [[1, 1, 0, 2, 2], [1, 1, 1, 0, 0]]
+
+
+def test_cpu_baseline_sample_is_bounded_and_reported():
+    """The oracle sample stops once its time budget is spent (at least one
+    head) and says how many heads it timed."""
+    cfg = CONFIGS["tiny"].with_(n=64, steps=4)
+    rep = bench.cpu_baseline(cfg, max_heads=3, budget_s=0.0)
+    assert rep["kind"] == "oracle" and rep["value"] > 0 and rep["cores"] >= 1
+    assert rep["sample"].startswith("1 of 4 heads")
+    full = bench.cpu_baseline(cfg, max_heads=3, budget_s=None)
+    assert full["sample"].startswith("3 of 4 heads")

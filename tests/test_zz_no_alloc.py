@@ -5,8 +5,14 @@ e.g. an engine whose pool allocator took all free device memory at start-up.
 Its scratch is a fixed array inside the library instead of a caller-supplied
 workspace.  The GPU test drives it through the C ABI for two generation steps
 in a row, next to the ordinary entry point on an identical copy of the
-caches, and requires the same outputs (bf16 tolerance of the parity tests)
-and the same cache updates.  This file is collected last on purpose.
+caches.  Both run the same kernels on the same inputs, so the outputs, the
+K/V pools, the positions and the descriptors must agree bit for bit.
+
+The file name sorts last so that pytest collects it after every other test
+file: if it fails, a run that stops at the first failure (-x) has already run
+the rest of the suite.  The test makes the entry point's first call itself
+(the call that sets the array aside), so it passes alone in a fresh process
+and after the other tests alike.
 """
 import ctypes
 
@@ -16,9 +22,6 @@ import torch
 
 from adaptive_head_kv_gb300 import fastgen as fg
 from synth import CONFIGS, make_workload, punct_ids, special_ids
-
-BF16_ATOL = 2e-2  # the decode tolerance of the bf16 parity tests
-
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
     """Host-side check (no GPU needed): a plan whose partials exceed the
@@ -59,10 +62,12 @@ def test_noalloc_matches_workspace_decode_two_calls():
                                        noa.pos_pool, q, k, v, tid, noa.special, noa.punct, t,
                                        got, noa.dev_err)
         torch.cuda.synchronize()
-        got = got.float()
-        assert torch.isfinite(got).all()
-        assert (got - want).abs().max().item() <= BF16_ATOL, st
+        assert torch.isfinite(got.float()).all()
+        # same kernels, same inputs: only the scratch address differs
+        assert torch.equal(got.float(), want), st
     assert fg.fastgen_read_error(noa.dev_err) == fg.FG_OK
     assert torch.equal(ref.pos_pool, noa.pos_pool)
+    assert torch.equal(ref.K_pool, noa.K_pool)
+    assert torch.equal(ref.V_pool, noa.V_pool)
     assert np.array_equal(np.frombuffer(bytes(ref.descriptors()), dtype=np.uint8),
                           np.frombuffer(bytes(noa.descriptors()), dtype=np.uint8))
