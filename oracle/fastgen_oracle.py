@@ -369,3 +369,64 @@ def prompt_attention(Q, K, V, scale=None):
     A = attention_map(Q, np.asarray(K, dtype=np.float64), s)
     return A @ np.asarray(V, dtype=np.float64)
 
+
+
+# --- long prompts: the same profile with the map formed a block of rows at a time
+
+def attention_rows(Q, K, scale, lo, hi):
+    """Rows lo..hi-1 of A = softmax(s Q K^T) under the causal mask, each row
+    formed as in attention_map: row i depends only on q_i and k_0..k_i, so
+    the rows are returned over the key columns 0..hi-1 (every later key is
+    masked out of all of them).  [hi - lo, hi] float64."""
+    S = scale * (Q[lo:hi] @ K[:hi].T)
+    i = np.arange(lo, hi)[:, None]
+    j = np.arange(hi)[None, :]
+    S[j > i] = -np.inf
+    S = S - S.max(axis=1, keepdims=True)
+    E = np.exp(S)
+    return E / E.sum(axis=1, keepdims=True)
+
+
+def local_rows_block(lo, hi, w):
+    """Rows lo..hi-1 of the C_local mask {j : i - w < j <= i} (R4) over the
+    key columns 0..hi-1."""
+    i = np.arange(lo, hi)[:, None]
+    j = np.arange(hi)[None, :]
+    return (j <= i) & (j > i - w)
+
+
+def profile_head_long(Q, K, ids, special_ids, punct_ids, T, r_l, r_f, scale=None, block=512):
+    """profile_head for prompts whose [n, n] map does not fit in memory.
+
+    The definitions are those of profile_head (Method: A = softmax(QK^T),
+    base policies, shortlist, eq. (C*); readings R1-R6); only the map is
+    formed `block` query rows at a time, twice: the first sweep adds the
+    rows into the cumulative scores colsum_j = sum_i A_ij, which fix
+    C_frequent; the second sums each row's attention over the per-row kept
+    sets K_i^p of the four compressed entries.  Returns the dict of
+    profile_head without A."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    n, d = Q.shape
+    s = default_scale(d) if scale is None else scale
+    w, k = ratio_count(r_l, n), ratio_count(r_f, n)
+    colsum = np.zeros(n)
+    for lo in range(0, n, block):
+        hi = min(lo + block, n)
+        colsum[:hi] += attention_rows(Q, K, s, lo, hi).sum(axis=0)
+    spec, punc = token_sets(ids[:n], special_ids, punct_ids)
+    freq = frequent_set(colsum, k)
+    static = [spec, spec | punc, spec | punc | freq]
+    kept = np.zeros(4)
+    for lo in range(0, n, block):
+        hi = min(lo + block, n)
+        A = attention_rows(Q, K, s, lo, hi)
+        for p in range(3):  # sum_i sum_j A_ij [j in K^p]
+            kept[p] += (A @ static[p][:hi].astype(np.float64)).sum()
+        kept[3] += (A * (static[2][None, :hi] | local_rows_block(lo, hi, w))).sum()
+    mass = [float(x / n) for x in kept] + [1.0]
+    finals = final_sets(n, spec, punc, freq, w)
+    cost = [int((f != DROP).sum()) for f in finals]
+    p = choose_policy(mass, cost, T)
+    return dict(policy=p, mass=np.array(mass), cost=np.array(cost), colsum=colsum,
+                keep=finals[p], kept=cost[p], w=w, k=k, freq=freq)

@@ -8,3 +8,19 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the sm_103a kernels)")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """How many compared heads each tolerance exemption took, per workload
+    (policy: an oracle mass within 1e-5 of T; top-k: an oracle top-k gap
+    within 1e-5 relative)."""
+    mod = sys.modules.get("parity_util")
+    reports = getattr(mod, "REPORTS", None) if mod else None
+    if not reports:
+        return
+    terminalreporter.write_sep("-", "parity exemptions per workload")
+    for name, rep in reports:
+        if rep["checked"]:
+            terminalreporter.write_line(
+                f"{name}: {rep['checked']} heads compared, {rep['decode_checked']} decoded, "
+                f"policy-exempt {rep['policy_exempt']}, top-k-exempt {rep['topk_exempt']}")

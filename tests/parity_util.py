@@ -7,7 +7,10 @@ Tolerances (stated once, used by every parity test):
     lies within NEAR of T, and from the kept-set check when its oracle colsum
     gap at the top-k boundary is within NEAR (relative to max(1, value)).
     Exempt heads must still make a valid choice (checked).
-  * colsum and masses: |gpu - oracle| <= RTOL |oracle| + ATOL, RTOL = 1e-4.
+  * colsum and masses: |gpu - oracle| <= RTOL |oracle| + ATOL, # every compare() call's counts, printed at the end of the test session
+REPORTS: list = []
+
+RTOL = 1e-4.
     The absolute floor covers values below what fp32 sums of probabilities
     resolve (e.g. 1e-40 attention on a masked-out special token).
   * decode outputs: 2e-2 absolute for bf16, 1e-5 for fp32, on every head
@@ -15,11 +18,17 @@ Tolerances (stated once, used by every parity test):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 from oracle import fastgen_oracle as O
+from oracle_pool import oracle_job
 from synth import make_workload, punct_ids, special_ids
+
+# every compare() call's counts, printed at the end of the test session
+REPORTS: list = []
 
 RTOL = 1e-4
 COLSUM_ATOL = 1e-6
@@ -101,6 +110,38 @@ def oracle_head(cfg, w, idx, T=None):
     return r
 
 
+def oracle_heads(cfg, w, idxs, T=None, long_prompt=False, procs=None):
+    """Oracle results of several heads of the workload, computed in parallel
+    by spawned worker processes (never forked: the caller holds a CUDA
+    context).  long_prompt selects the row-block profile (prompts whose dense
+    map does not fit in host memory).  Returns {idx: result}."""
+    import multiprocessing as mp
+
+    T = float(np.float32(cfg.T if T is None else T))
+    jobs = []
+    for idx in idxs:
+        g = int(w["heads"][idx])
+        b = g // (cfg.L * cfg.H)
+        jobs.append((w["Q"][idx].double().numpy(), w["K"][idx].double().numpy(),
+                     w["V"][idx].double().numpy(), w["ids"][b], cfg.n, cfg.steps, T, cfg.r_l,
+                     cfg.r_f, long_prompt))
+    procs = procs or max(1, min(len(jobs), (os.cpu_count() or 2) // 2))
+    threads = str(max(1, (os.cpu_count() or 1) // procs))
+    keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    os.environ.update({k: threads for k in keys})  # read by the workers' BLAS at start-up
+    try:
+        with mp.get_context("spawn").Pool(procs) as pool:
+            res = pool.map(oracle_job, jobs, chunksize=1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return dict(zip(idxs, res))
+
+
 def close(a, b, rtol, atol):
     return np.abs(a - b) <= rtol * np.abs(b) + atol
 
@@ -122,9 +163,11 @@ def cache_positions(desc, pos_pool):
     return np.array(sorted(list(st) + [x for x in ring if x >= 0]), dtype=np.int64)
 
 
-def compare(cfg, gpu, heads_idx, T=None, report=None):
+def compare(cfg, gpu, heads_idx, T=None, report=None, oracle=None):
     """Compares sampled heads (indices into the workload) and the all-head
-    invariants.  Returns a dict of counts; raises AssertionError on a miss."""
+    invariants.  `oracle` optionally holds the heads' oracle results
+    ({idx: result}, e.g. from oracle_heads); otherwise each head's is
+    computed here.  Returns a dict of counts; raises AssertionError on a miss."""
     w = gpu["workload"]
     T = float(np.float32(cfg.T if T is None else T))
     n = cfg.n
@@ -146,7 +189,7 @@ def compare(cfg, gpu, heads_idx, T=None, report=None):
     atol_dec = dec_atol(cfg.dtype)
     for idx in heads_idx:
         g = int(w["heads"][idx])
-        ora = oracle_head(cfg, w, idx, T)
+        ora = oracle[idx] if oracle is not None else oracle_head(cfg, w, idx, T)
         rep["checked"] += 1
         cs_ok = close(gpu["colsum"][g], ora["colsum"], RTOL, COLSUM_ATOL)
         assert cs_ok.all(), (g, np.nonzero(~cs_ok)[0][:5])
@@ -202,6 +245,8 @@ def compare(cfg, gpu, heads_idx, T=None, report=None):
         rep["decode_checked"] += 1
     if report is not None:
         report.update(rep)
+    REPORTS.append((f"{cfg.name} B={cfg.B} L={cfg.L} H={cfg.H} n={cfg.n} d={cfg.d} "
+                    f"{cfg.dtype} T={T:g}", dict(rep)))
     return rep
 
 

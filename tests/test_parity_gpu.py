@@ -111,13 +111,14 @@ def test_deterministic_rerun():
 
 
 def test_long32k_full_length_properties():
-    """The 32k-token prompt at full length (d = 128), one head of each type.
-    The oracle's dense map is too slow at this size, so the check uses what
-    holds at any size: every all-head invariant of the comparison, the planted
-    special head choosing the special-only cache and the planted local head a
-    local-containing one, and the closed form of the special head's decode
-    output (its cache holds only the BOS row unless a special token arrives,
-    so the output is that row's value vector)."""
+    """The 32k-token prompt at full length (d = 128), one planted head of
+    each type: properties that hold at any size (every all-head invariant of
+    the comparison, the planted special head choosing the special-only cache
+    and the planted local head a local-containing one, and the closed form of
+    the special head's decode output: its cache holds only the BOS row unless
+    a special token arrives, so the output is that row's value vector).  The
+    element-by-element comparison at this length is
+    test_long32k_full_size_sampled."""
     import numpy as np
 
     from synth import special_ids
@@ -179,16 +180,14 @@ class _HeadColumns:
         return self.outs[:, g].float().cpu().numpy().astype(np.float64)
 
 
-def test_llama65b_full_size_sampled():
-    """The largest workload at full size (G = 40960 heads, n = 2048, 1024
-    decode steps, CUDA-graph decode as the benchmark runs it): every head's
-    invariants, then sampled heads of every type, first and last layer,
-    against the oracle.  The sampled heads are regenerated on their own, so
-    host memory holds the prompt/decode layout once."""
+def run_full_size(cfg):
+    """The whole workload on the GPU as the bench runs it (prefill, then
+    every decode step replayed as one CUDA graph).  Returns the host copies
+    compared (decode outputs stay on the device, read per head) and the
+    head types."""
     from adaptive_head_kv_gb300.session import FastGenSession, make_params
-    from synth import make_workload, make_workload_split, punct_ids, special_ids
+    from synth import make_workload_split, punct_ids, special_ids
 
-    cfg = CONFIGS["llama65b"]
     n, steps, dev = cfg.n, cfg.steps, torch.device("cuda")
     w = make_workload_split(cfg)
     p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
@@ -206,9 +205,66 @@ def test_llama65b_full_size_sampled():
                mass=s.mass.cpu().numpy().astype(np.float64), cost=s.cost.cpu().numpy(),
                colsum=s.colsum.cpu().numpy().astype(np.float64), keep=s.keep.cpu().numpy(),
                kept=s.kept.cpu().numpy(), out=_HeadColumns(outs), desc1=s.descriptors(),
-               pos1=s.pos_pool.cpu().numpy())
-    assert int(s.dev_err.item()) == 0
-    heads = sample_heads(cfg, w["types"], 16)
+               pos1=s.pos_pool.cpu().numpy(), dev_err=int(s.dev_err.item()))
+    return gpu, w["types"]
+
+
+def test_llama65b_full_size_sampled():
+    """The largest workload at full size (G = 40960 heads, n = 2048, 1024
+    decode steps, CUDA-graph decode as the benchmark runs it): every head's
+    invariants, then sampled heads of every type, first and last layer,
+    against the oracle.  The sampled heads are regenerated on their own, so
+    host memory holds the prompt/decode layout once."""
+    from synth import make_workload
+
+    cfg = CONFIGS["llama65b"]
+    gpu, types = run_full_size(cfg)
+    assert gpu["dev_err"] == 0
+    heads = sample_heads(cfg, types, 16)
     gpu["workload"] = make_workload(cfg, heads=heads)
     rep = compare(cfg, gpu, range(len(heads)))
     assert rep["decode_checked"] >= 10, rep
+
+
+def test_llama13b_full_size_sampled():
+    """The 13B workload at its own batch (B = 4 sequences, 40 layers of 40
+    heads, n = 4096, 512 decode steps, CUDA-graph decode): every head's
+    invariants, then sampled heads of every type, first and last layer, and
+    of every sequence, against the oracle element by element."""
+    from parity_util import oracle_heads
+    from synth import make_workload
+
+    cfg = CONFIGS["llama13b"]
+    gpu, types = run_full_size(cfg)
+    assert gpu["dev_err"] == 0
+    heads = set(sample_heads(cfg, types, 12))
+    for b in range(cfg.B):  # each sequence's first and last layer
+        heads.add(b * cfg.L * cfg.H + (b % cfg.H))
+        heads.add((b * cfg.L + cfg.L - 1) * cfg.H + (b % cfg.H))
+    heads = sorted(heads)
+    gpu["workload"] = make_workload(cfg, heads=heads)
+    ora = oracle_heads(cfg, gpu["workload"], list(range(len(heads))))
+    rep = compare(cfg, gpu, range(len(heads)), oracle=ora)
+    print("llama13b", rep)
+    assert rep["decode_checked"] >= len(heads) // 2, rep
+
+
+def test_long32k_full_size_sampled():
+    """The 32k-token workload at full size (1024 heads, n = 32768, d = 128,
+    256 decode steps, CUDA-graph decode): every head's invariants, then
+    sampled heads of every type, first and last layer, against the oracle's
+    row-block profile (the dense map of one head would take 8.6 GB) and its
+    decode: column sums, masses, policy, keep codes, every decode output and
+    the final cache positions."""
+    from parity_util import oracle_heads
+    from synth import make_workload
+
+    cfg = CONFIGS["long32k"]
+    gpu, types = run_full_size(cfg)
+    assert gpu["dev_err"] == 0
+    heads = sample_heads(cfg, types, 8)
+    gpu["workload"] = make_workload(cfg, heads=heads)
+    ora = oracle_heads(cfg, gpu["workload"], list(range(len(heads))), long_prompt=True)
+    rep = compare(cfg, gpu, range(len(heads)), oracle=ora)
+    print("long32k", rep)
+    assert rep["decode_checked"] >= len(heads) // 2, rep
