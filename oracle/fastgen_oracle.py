@@ -430,3 +430,107 @@ def profile_head_long(Q, K, ids, special_ids, punct_ids, T, r_l, r_f, scale=None
     p = choose_policy(mass, cost, T)
     return dict(policy=p, mass=np.array(mass), cost=np.array(cost), colsum=colsum,
                 keep=finals[p], kept=cost[p], w=w, k=k, freq=freq)
+
+
+# --- decode-time refresh of C_frequent (reading R13, off unless asked for) ---
+# The pages define C_frequent by the largest cumulative attention scores and,
+# in the stability paragraph, track accumulated attention over the prompt and
+# later decoding steps; they reuse the prompt-time policy and state no rule
+# for updating the frequent set while generating.  R13 is this build's own
+# rule for such an update, available only on request (period > 0):
+#   * every cached row j carries an accumulated score acc_j: its prompt
+#     column sum colsum_j at the end of the prompt (0 for a generated token
+#     when it is placed), plus, at every step, the attention weight the
+#     step's query gives it (the softmax over the cache after placement);
+#   * after every `period`-th generation step, the frequent members F (the
+#     never-evicted rows kept for frequency, i.e. not special or punctuation
+#     tokens) are re-chosen as the |F| rows of largest acc among F and the
+#     non-special, non-punctuation rows of the current local window (ties to
+#     the lower position); |F| never changes, so neither does the cache size;
+#   * a member that loses its place leaves the cache, unless it is inside
+#     the window, where it stays until it is w positions old like any window
+#     row; a window row that wins a place stays in the cache for good;
+#     dropped rows never return.
+# Only local-hybrid caches have window rows to promote: for the other
+# entries the refresh leaves the cache as profiled.
+
+def accumulate_scores(acc, pos, weights):
+    """acc_j += the step's attention weight of cached row j (R13)."""
+    for j, a in zip(pos, weights):
+        acc[int(j)] = acc.get(int(j), 0.0) + float(a)
+
+
+def refresh_frequent(freq, window_candidates, acc):
+    """R13: the |F| rows of largest accumulated score among the frequent
+    members and the window candidates, ties to the lower position."""
+    cand = sorted(set(freq) | set(window_candidates), key=lambda j: (-acc[j], j))
+    return set(cand[:len(freq)])
+
+
+def refresh_cache_positions(policy, static_sp, freq, w, t):
+    """Cache positions at step t under R13: never-evicted special/punct
+    members, the frequent members and, for the local hybrid, the window."""
+    pos = set(int(p) for p in static_sp) | set(int(p) for p in freq)
+    if policy == P_SPFL:
+        pos.update(range(max(t - w + 1, 0), t + 1))
+    return np.array(sorted(pos), dtype=np.int64)
+
+
+def attention_weights(q, Kc, scale):
+    """softmax(s q K_c^T) over the cache rows (the weights attend() applies)."""
+    s = scale * (np.asarray(Kc, dtype=np.float64) @ np.asarray(q, dtype=np.float64))
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def decode_head_refresh(policy, keep, n, w, ids, Qall, Kall, Vall, special_ids, punct_ids,
+                        steps, colsum, period, scale=None):
+    """decode_head with the frequent set refreshed every `period` steps by
+    R13 (period 0: never, which is decode_head).  colsum: the prompt's
+    cumulative scores [n].  Returns dict(out [steps, d], pos: positions seen
+    at the last step, final: the cache after the last refresh, acc: final
+    accumulated scores of the cached rows, gaps: per refresh, the score gap
+    between the last member kept and the best candidate left out, relative
+    to max(1, score) (inf when nothing was left out))."""
+    Kall = np.asarray(Kall, dtype=np.float64)
+    Vall = np.asarray(Vall, dtype=np.float64)
+    Qall = np.asarray(Qall, dtype=np.float64)
+    d = Kall.shape[1]
+    s = default_scale(d) if scale is None else scale
+    sset, pset = set(int(x) for x in special_ids), set(int(x) for x in punct_ids)
+    keep = np.asarray(keep)
+    is_sp = lambda j: int(ids[j]) in sset or int(ids[j]) in pset
+    static = [int(j) for j in np.nonzero(keep == KEEP_STATIC)[0]]
+    uses_f = policy in (P_SPF, P_SPFL)
+    static_sp = [j for j in static if is_sp(j) or not uses_f]
+    freq = set(j for j in static if uses_f and not is_sp(j))
+    acc = {int(j): float(colsum[j]) for j in np.nonzero(keep != DROP)[0]}
+    out = np.zeros((steps, d))
+    gaps = []
+    pos = refresh_cache_positions(policy, static_sp, freq, w, n - 1)
+    for step in range(steps):
+        t = n + step
+        tau = int(ids[t])
+        if stores_static(policy, tau in sset, tau in pset):
+            static_sp.append(t)
+        pos = refresh_cache_positions(policy, static_sp, freq, w, t)
+        if len(pos):
+            acc.setdefault(t, 0.0)
+            a = attention_weights(Qall[t], Kall[pos], s)
+            out[step] = a @ Vall[pos]
+            accumulate_scores(acc, pos, a)
+        if period > 0 and uses_f and (step + 1) % period == 0:
+            window = range(max(t - w + 1, 0), t + 1) if policy == P_SPFL else range(0)
+            cands = [j for j in window if not is_sp(j)]
+            new = refresh_frequent(freq, cands, acc)
+            ranked = sorted(set(freq) | set(cands), key=lambda j: (-acc[j], j))
+            kf = len(freq)
+            if 0 < kf < len(ranked):
+                hi, lo = acc[ranked[kf - 1]], acc[ranked[kf]]
+                gaps.append((hi - lo) / max(1.0, hi))
+            else:
+                gaps.append(math.inf)
+            freq = new
+    final = refresh_cache_positions(policy, static_sp, freq, w, n + steps - 1)
+    return dict(out=out, pos=pos, final=final,
+                acc={int(j): acc[int(j)] for j in final}, gaps=gaps)
