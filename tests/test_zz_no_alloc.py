@@ -67,7 +67,8 @@ def test_noalloc_matches_workspace_decode_two_calls():
         assert torch.equal(got.float(), want), st
     assert fg.fastgen_read_error(noa.dev_err) == fg.FG_OK
     assert torch.equal(ref.pos_pool, noa.pos_pool)
-    assert torch.equal(ref.K_pool, noa.K_pool)
-    assert torch.equal(ref.V_pool, noa.V_pool)
+    live = ref.pos_pool >= 0  # rows in use; empty rows hold unspecified bytes
+    assert torch.equal(ref.K_pool[live], noa.K_pool[live])
+    assert torch.equal(ref.V_pool[live], noa.V_pool[live])
     assert np.array_equal(np.frombuffer(bytes(ref.descriptors()), dtype=np.uint8),
                           np.frombuffer(bytes(noa.descriptors()), dtype=np.uint8))
