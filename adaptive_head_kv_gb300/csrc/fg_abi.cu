@@ -265,13 +265,15 @@ size_t fastgen_decode_workspace_bytes(const fg_params* p, const fg_plan_info* in
   return align_up(nw * 2 * sizeof(float)) + align_up(nw * p->d * sizeof(float));
 }
 
-fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info* info,
-                              void* K_pool, void* V_pool, int32_t* pos_pool, const void* q,
-                              const void* k_new, const void* v_new, const int32_t* new_ids,
-                              const int32_t* special_ids, int32_t n_special,
-                              const int32_t* punct_ids, int32_t n_punct, int32_t pos,
-                              void* out, void* workspace, size_t workspace_bytes,
-                              int32_t* dev_err, void* stream) {
+// Shared by fastgen_decode_attn and fastgen_decode_attn_refresh (row_acc and
+// row_sc non-null: every row's attention weight is added to its score).
+static fg_status decode_call(const fg_params* p, void* plan, const fg_plan_info* info,
+                             void* K_pool, void* V_pool, int32_t* pos_pool, const void* q,
+                             const void* k_new, const void* v_new, const int32_t* new_ids,
+                             const int32_t* special_ids, int32_t n_special,
+                             const int32_t* punct_ids, int32_t n_punct, int32_t pos, void* out,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                             float* row_acc, float* row_sc, void* stream) {
   fg_status st = check_params(p);
   if (st != FG_OK) return st;
   if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
@@ -308,12 +310,96 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
   a.part_ml = (float*)ws;
   a.part_acc = (float*)(ws + align_up((size_t)info->n_work * pd.R * 2 * sizeof(float)));
   a.dev_err = dev_err;
+  a.row_acc = row_acc;
+  a.row_sc = row_sc;
   if (info->n_work == 0) {
     cudaError_t e = cudaMemsetAsync(out, 0, (size_t)pd.G * pd.d * elem_bytes(p),
                                     (cudaStream_t)stream);
     return cuda_status(e);
   }
   return cuda_status(fg::launch_decode(pd, a, (cudaStream_t)stream));
+}
+
+fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info* info,
+                              void* K_pool, void* V_pool, int32_t* pos_pool, const void* q,
+                              const void* k_new, const void* v_new, const int32_t* new_ids,
+                              const int32_t* special_ids, int32_t n_special,
+                              const int32_t* punct_ids, int32_t n_punct, int32_t pos,
+                              void* out, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, void* stream) {
+  return decode_call(p, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new, new_ids,
+                     special_ids, n_special, punct_ids, n_punct, pos, out, workspace,
+                     workspace_bytes, dev_err, nullptr, nullptr, stream);
+}
+
+// Refresh state: [acc f32 x pool_rows][sc f32 x pool_rows][role u8 x pool_rows].
+size_t fastgen_refresh_state_bytes(const fg_params* p, const fg_plan_info* info) {
+  if (check_params(p) != FG_OK || !info || info->pool_rows < 0) return 0;
+  const size_t rows = (size_t)info->pool_rows;
+  return 2 * align_up(rows * sizeof(float)) + align_up(rows);
+}
+
+static fg_status check_refresh(const fg_params* p, const fg_plan_info* info, const void* state,
+                               size_t state_bytes) {
+  fg_status st = check_params(p);
+  if (st != FG_OK) return st;
+  if (group_size(p) != 1) return FG_EINVAL;  // one query per cache only
+  if ((long long)ratio_count(p->r_l, p->n) + ratio_count(p->r_f, p->n) >
+      fg::kRefreshMaxCandidates)
+    return FG_EINVAL;
+  if (!info || !state || !aligned(state, kAlign)) return FG_EINVAL;
+  if (state_bytes < fastgen_refresh_state_bytes(p, info)) return FG_EWORKSPACE;
+  return FG_OK;
+}
+
+fg_status fastgen_refresh_init(const fg_params* p, const void* plan, const fg_plan_info* info,
+                               const int32_t* pos_pool, const float* colsum,
+                               const int32_t* token_ids, const int32_t* special_ids,
+                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                               void* state, size_t state_bytes, void* stream) {
+  fg_status st = check_refresh(p, info, state, state_bytes);
+  if (st != FG_OK) return st;
+  if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
+  if ((st = check_ids(punct_ids, n_punct)) != FG_OK) return st;
+  if (!plan || !pos_pool || !colsum || !token_ids || !aligned(plan, kAlign) ||
+      !aligned(pos_pool, 4) || !aligned(colsum, 4) || !aligned(token_ids, 4))
+    return FG_EINVAL;
+  const fg::ProfileDims pd = dims(p);
+  const size_t rows = (size_t)info->pool_rows;
+  char* sb = (char*)state;
+  float* acc = (float*)sb;
+  uint8_t* role = (uint8_t*)(sb + 2 * align_up(rows * sizeof(float)));
+  return cuda_status(fg::launch_refresh_init(pd, (const fg_head_desc*)plan, pos_pool, colsum,
+                                             token_ids, special_ids, n_special, punct_ids,
+                                             n_punct, acc, role, (cudaStream_t)stream));
+}
+
+fg_status fastgen_decode_attn_refresh(const fg_params* p, void* plan, const fg_plan_info* info,
+                                      void* K_pool, void* V_pool, int32_t* pos_pool,
+                                      const void* q, const void* k_new, const void* v_new,
+                                      const int32_t* new_ids, const int32_t* special_ids,
+                                      int32_t n_special, const int32_t* punct_ids,
+                                      int32_t n_punct, int32_t pos, int32_t period, void* out,
+                                      void* state, size_t state_bytes, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  fg_status st = check_refresh(p, info, state, state_bytes);
+  if (st != FG_OK) return st;
+  if (period < 1) return FG_EINVAL;
+  const size_t rows = (size_t)info->pool_rows;
+  char* sb = (char*)state;
+  float* acc = (float*)sb;
+  float* sc = (float*)(sb + align_up(rows * sizeof(float)));
+  const uint8_t* role = (const uint8_t*)(sb + 2 * align_up(rows * sizeof(float)));
+  st = decode_call(p, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new, new_ids,
+                   special_ids, n_special, punct_ids, n_punct, pos, out, workspace,
+                   workspace_bytes, dev_err, acc, sc, stream);
+  if (st != FG_OK || info->n_work == 0) return st;
+  if ((pos - p->n + 1) % period != 0) return FG_OK;
+  const fg::ProfileDims pd = dims(p);
+  int cap = 2;
+  while (cap < pd.k + pd.w) cap <<= 1;
+  return cuda_status(fg::launch_refresh(pd, (fg_head_desc*)plan, K_pool, V_pool, pos_pool, acc,
+                                        role, pos, cap, (cudaStream_t)stream));
 }
 
 fg_status fastgen_read_error(const int32_t* dev_err, void* stream) {

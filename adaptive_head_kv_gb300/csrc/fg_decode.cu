@@ -98,7 +98,10 @@ __device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi
       *reinterpret_cast<uint4*>(Kp + d) = *reinterpret_cast<const uint4*>(kn + v * E);
       *reinterpret_cast<uint4*>(Vp + d) = *reinterpret_cast<const uint4*>(vn + v * E);
     }
-    if (threadIdx.x == 0) a.posp[m.base + m.new_slot] = a.pos;
+    if (threadIdx.x == 0) {
+      a.posp[m.base + m.new_slot] = a.pos;
+      if (a.row_acc) a.row_acc[m.base + m.new_slot] = 0.f;  // a generated token starts at 0
+    }
   }
   if (m.evict >= m.r0 && m.evict < m.r1 && threadIdx.x == 0) a.posp[m.base + m.evict] = -1;
   return m;
@@ -106,9 +109,11 @@ __device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi
 
 // R = queries per cache (group size).  Rows are unrolled by U per warp so
 // that 2 * U 16-byte loads per thread are in flight.
-template <typename T, int D, int R>
+// kAcc (one query per cache): also write every row's score to a.row_sc.
+template <typename T, int D, int R, bool kAcc = false>
 __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, int H, int HLkv,
                                                            float sl2) {
+  static_assert(!kAcc || R == 1, "row scores are kept for single-query caches only");
   constexpr int E = Vec16<T>::kElems;
   constexpr int LPR = D / E;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp per load
@@ -199,6 +204,10 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
           dot = (Score)df;
         }
         sc[u][q] = ok[u] ? dot : (Score)FG_NEG_INF;
+      }
+      if constexpr (kAcc) {
+        const int r = rb + (u * kDecWarps + warp) * RPW + grp;
+        if (gl == 0 && r < r1) a.row_sc[base + r] = (float)sc[u][0];
       }
     }
 #pragma unroll
@@ -585,7 +594,9 @@ __global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeA
 // forms the item weights itself (a few exp2 per item, from broadcast loads)
 // and sums its dimension over the items, so each item costs one coalesced
 // row load for the whole CTA.
-template <typename T, int D>
+// kAcc: also add each cached row's final attention weight 2^(sc - M) / L to
+// its accumulated score (one query per cache).
+template <typename T, int D, bool kAcc = false>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, int R, int HLkv) {
   griddep_wait();
   griddep_launch_dependents();
@@ -630,6 +641,33 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
     const Placement pl = place(hd, a, HLkv, c);
     if (pl.st) a.desc[c].n_static = hd.n_static + 1;
   }
+  if constexpr (kAcc) {
+    if (M != FG_NEG_INF && L > 0.f) {
+      const float inv = 1.f / L;
+      const Placement pl = place(hd, a, HLkv, c);
+      const int ns = hd.n_static + (pl.st ? 1 : 0);
+      for (int r = t; r < ns; r += D) {
+        const long long row = hd.off + r;
+        const float sv = a.row_sc[row];
+        if (sv != FG_NEG_INF) a.row_acc[row] += exp2f(sv - M) * inv;
+      }
+      for (int r = t; r < hd.w; r += D) {
+        const long long row = hd.win_off + r;
+        const float sv = a.row_sc[row];
+        if (sv != FG_NEG_INF) a.row_acc[row] += exp2f(sv - M) * inv;
+      }
+    }
+  }
+}
+
+// Single-query caches with accumulated row scores (refresh of C_frequent).
+template <typename T, int D>
+cudaError_t run_acc(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
+  cudaError_t e = launch_pdl(split_kernel<T, D, 1, true>, a.n_work, kDecThreads, 0, s, a, pd.H,
+                             pd.HLkv, pd.sl2);
+  if (e == cudaSuccess)
+    e = launch_pdl(combine_kernel<T, D, true>, pd.G, D, 0, s, a, pd.H, pd.R, pd.HLkv);
+  return e;
 }
 
 template <typename T, int D, int R>
@@ -664,6 +702,13 @@ cudaError_t run_r(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
+  if (a.row_acc) {
+    if (pd.R != 1 || !a.row_sc) return cudaErrorInvalidValue;
+    if (pd.dtype == FG_FP32)
+      return pd.d == 64 ? run_acc<float, 64>(pd, a, s) : run_acc<float, 128>(pd, a, s);
+    return pd.d == 64 ? run_acc<__nv_bfloat16, 64>(pd, a, s)
+                      : run_acc<__nv_bfloat16, 128>(pd, a, s);
+  }
   if (pd.dtype == FG_FP32)
     return pd.d == 64 ? run_r<float, 64>(pd, a, s) : run_r<float, 128>(pd, a, s);
   return pd.d == 64 ? run_r<__nv_bfloat16, 64>(pd, a, s) : run_r<__nv_bfloat16, 128>(pd, a, s);

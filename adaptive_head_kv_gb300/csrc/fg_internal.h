@@ -102,8 +102,27 @@ struct DecodeArgs {
   float* part_ml;   // [n_work, R, 2]
   float* part_acc;  // [n_work, R, d]
   int32_t* dev_err;
+  // accumulated attention of every pool row (refresh of C_frequent; no groups):
+  // when non-null the split kernel writes each row's score to row_sc and the
+  // combine adds its final weight to row_acc
+  float* row_acc = nullptr;
+  float* row_sc = nullptr;
 };
 
 cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s);
+
+// Refresh of C_frequent (opt-in).  Init: per pool row, acc = the prompt column
+// sum of its position (0 for empty rows) and role = 1 for never-evicted rows
+// kept for frequency.  Refresh: one CTA per cache re-chooses the frequent
+// members among them and the window rows (cap: shared key slots, a power of
+// two >= k + w; t: the step's position).
+constexpr int kRefreshMaxCandidates = 16384;
+cudaError_t launch_refresh_init(const ProfileDims& pd, const fg_head_desc* desc,
+                                const int32_t* posp, const float* colsum, const int32_t* ids,
+                                const int32_t* special, int ns, const int32_t* punct, int np,
+                                float* acc, uint8_t* role, cudaStream_t s);
+cudaError_t launch_refresh(const ProfileDims& pd, fg_head_desc* desc, void* Kp, void* Vp,
+                           int32_t* posp, float* acc, const uint8_t* role, int t, int cap,
+                           cudaStream_t s);
 
 }  // namespace fg

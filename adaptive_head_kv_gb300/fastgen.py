@@ -23,13 +23,15 @@ FG_KEEP_DROP, FG_KEEP_STATIC, FG_KEEP_WINDOW = 0, 1, 2
 
 # kernels launched by one call of each entry point (counted in the bench)
 LAUNCHES = {"profile": 4, "profile_attn": 5, "profile_with_policy": 5, "plan": 3, "compact": 1,
-            "decode": 2}
+            "decode": 2, "decode_refresh": 3, "refresh_init": 1}
 
 EXPORTS = (
     "fastgen_status_string", "fastgen_version", "fastgen_profile_workspace_bytes",
     "fastgen_profile", "fastgen_plan_bytes", "fastgen_compact_plan", "fastgen_compact",
     "fastgen_decode_workspace_bytes", "fastgen_decode_attn", "fastgen_read_error",
     "fastgen_decode_attn_noalloc", "fastgen_profile_with_policy", "fastgen_profile_attn",
+    "fastgen_plan_compact", "fastgen_refresh_state_bytes", "fastgen_refresh_init",
+    "fastgen_decode_attn_refresh",
 )
 
 # size of the library-held scratch array used by fastgen_decode_attn_noalloc
@@ -87,6 +89,13 @@ _SIGS = {
                                            _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                            _P, _P, _SZ, _P, _P]),
     "fastgen_read_error": (ctypes.c_int, [_P, _P]),
+    "fastgen_refresh_state_bytes": (_SZ, [ctypes.POINTER(Params), ctypes.POINTER(PlanInfo)]),
+    "fastgen_refresh_init": (ctypes.c_int, [ctypes.POINTER(Params), _P, ctypes.POINTER(PlanInfo),
+                                            _P, _P, _P, _P, _I32, _P, _I32, _P, _SZ, _P]),
+    "fastgen_decode_attn_refresh": (ctypes.c_int, [ctypes.POINTER(Params), _P,
+                                                   ctypes.POINTER(PlanInfo), _P, _P, _P, _P, _P,
+                                                   _P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _P,
+                                                   _SZ, _P, _SZ, _P, _P]),
     "fastgen_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(Params), _P,
                                                    ctypes.POINTER(PlanInfo), _P, _P, _P, _P, _P,
                                                    _P, _P, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
@@ -245,3 +254,30 @@ def fastgen_decode_attn_noalloc(params, plan, info, K_pool, V_pool, pos_pool, q,
         _ptr(pos_pool), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(new_ids), _ptr(special_ids),
         _count(special_ids), _ptr(punct_ids), _count(punct_ids), int(pos), _ptr(out),
         _ptr(dev_err), _stream(stream)), "fastgen_decode_attn_noalloc")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def fastgen_refresh_state_bytes(params: Params, info: PlanInfo) -> int:
+    return lib().fastgen_refresh_state_bytes(ctypes.byref(params), ctypes.byref(info))
+
+
+def fastgen_refresh_init(params, plan, info, pos_pool, colsum, token_ids, special_ids, punct_ids,
+                         state, stream=None) -> None:
+    _check(lib().fastgen_refresh_init(
+        ctypes.byref(params), _ptr(plan), ctypes.byref(info), _ptr(pos_pool), _ptr(colsum),
+        _ptr(token_ids), _ptr(special_ids), _count(special_ids), _ptr(punct_ids),
+        _count(punct_ids), _ptr(state), _nbytes(state), _stream(stream)), "fastgen_refresh_init")
+
+
+def fastgen_decode_attn_refresh(params, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new,
+                                new_ids, special_ids, punct_ids, pos, period, out, state,
+                                workspace, dev_err, stream=None) -> None:
+    _check(lib().fastgen_decode_attn_refresh(
+        ctypes.byref(params), _ptr(plan), ctypes.byref(info), _ptr(K_pool), _ptr(V_pool),
+        _ptr(pos_pool), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(new_ids), _ptr(special_ids),
+        _count(special_ids), _ptr(punct_ids), _count(punct_ids), int(pos), int(period),
+        _ptr(out), _ptr(state), _nbytes(state), _ptr(workspace), _nbytes(workspace),
+        _ptr(dev_err), _stream(stream)), "fastgen_decode_attn_refresh")

@@ -26,11 +26,16 @@ GUARD_FILL = 0x5A
 class FastGenSession:
     """Owns the buffers of one batch of heads.  With guard=True every buffer
     the library writes gets GUARD_BYTES of canary bytes on both sides, and
-    check_guards() reports any that changed (a bounds check for tests)."""
+    check_guards() reports any that changed (a bounds check for tests).
+    refresh_period > 0 selects the opt-in refresh of the frequent sets every
+    that many generation steps (fastgen_decode_attn_refresh)."""
 
     def __init__(self, params: fg.Params, special_ids, punct_ids, max_new_tokens: int,
-                 device="cuda", stream=None, guard=False):
+                 device="cuda", stream=None, guard=False, refresh_period=0):
         self.p = params
+        self.refresh_period = int(refresh_period)
+        self.state = None
+        self._ids = None
         self.device = torch.device(device)
         self.stream = stream
         self.max_new = int(max_new_tokens)
@@ -60,6 +65,7 @@ class FastGenSession:
         self.dws = None
 
     def profile(self, Q, K, token_ids):
+        self._ids = token_ids
         fg.fastgen_profile(self.p, Q, K, token_ids, self.special, self.punct, self.policy,
                            self.mass, self.cost, self.colsum, self.keep, self.kept, self.ws,
                            self.dev_err, self.stream)
@@ -92,6 +98,7 @@ class FastGenSession:
                                                       self.pos_pool, self.stream)
             self._size_decode_workspace()
             if done:
+                self._init_refresh()
                 return
         else:
             self.info = fg.fastgen_compact_plan(self.p, self.policy, self.keep, self.max_new,
@@ -105,6 +112,17 @@ class FastGenSession:
         self._size_decode_workspace()
         fg.fastgen_compact(self.p, K, V, self.keep, self.plan, self.info, self.K_pool,
                            self.V_pool, self.pos_pool, self.stream)
+        self._init_refresh()
+
+    def _init_refresh(self):
+        """Accumulated scores and frequent slots of the new caches (refresh mode)."""
+        if self.refresh_period <= 0:
+            return
+        need = fg.fastgen_refresh_state_bytes(self.p, self.info)
+        if self.state is None or self.state.numel() < need:
+            self.state = self._empty((max(need, 256),), torch.uint8)
+        fg.fastgen_refresh_init(self.p, self.plan, self.info, self.pos_pool, self.colsum,
+                                self._ids, self.special, self.punct, self.state, self.stream)
 
     def _size_decode_workspace(self):
         need = fg.fastgen_decode_workspace_bytes(self.p, self.info)
@@ -143,10 +161,21 @@ class FastGenSession:
         """One generation step: q [G, d] per query head, k_new/v_new [Gkv, d]
         per key/value head, new_ids [B]; returns out [G, d]."""
         out = self.out if out is None else out
+        if self.refresh_period > 0:
+            fg.fastgen_decode_attn_refresh(self.p, self.plan, self.info, self.K_pool, self.V_pool,
+                                           self.pos_pool, q, k_new, v_new, new_ids, self.special,
+                                           self.punct, pos, self.refresh_period, out, self.state,
+                                           self.dws, self.dev_err, self.stream)
+            return out
         fg.fastgen_decode_attn(self.p, self.plan, self.info, self.K_pool, self.V_pool,
                                self.pos_pool, q, k_new, v_new, new_ids, self.special, self.punct,
                                pos, out, self.dws, self.dev_err, self.stream)
         return out
+
+    def row_scores(self):
+        """Accumulated score of every pool row (refresh mode; host copy)."""
+        rows = int(self.info.pool_rows)
+        return self.state[: rows * 4].view(torch.float32).cpu()
 
     def capture_decode(self, q, k, v, new_ids, pos0):
         """Captures len(q) consecutive decode calls (inputs q [steps, G, d],

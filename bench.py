@@ -475,14 +475,36 @@ def oracle_sample(cfg, heads, seed=0, budget_s=None):
 
 def blas_threads():
     """Threads of numpy's BLAS pool: the most threads the oracle uses at a
-    time (its matrix products); every other oracle step is single-threaded."""
+    time (its matrix products); every other oracle step is single-threaded.
+    Asked of threadpoolctl where installed, else of the OpenBLAS library
+    loaded in this process (its documented openblas_get_num_threads call)."""
     try:
         from threadpoolctl import threadpool_info
 
         return max([i.get("num_threads", 1) for i in threadpool_info()
                     if i.get("user_api") == "blas"] + [1])
     except Exception:
-        return 1
+        pass
+    import ctypes
+
+    np.ones((2, 2)) @ np.ones((2, 2))  # BLAS is loaded
+    try:
+        libs = sorted({f[-1] for f in (l.split() for l in open("/proc/self/maps"))
+                       if len(f) >= 6 and "openblas" in f[-1].lower() and ".so" in f[-1]})
+    except OSError:
+        libs = []
+    for path in libs:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                     "scipy_openblas_get_num_threads", "openblas_get_num_threads"):
+            fn = getattr(lib, name, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return max(1, int(fn()))
+    return os.cpu_count() or 1
 
 
 def cpu_baseline(cfg, max_heads=48, budget_s=20.0):

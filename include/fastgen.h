@@ -15,7 +15,9 @@
  * fastgen_profile_attn also returns the prompt attention output,
  * fastgen_profile_with_policy reuses a saved head-policy map),
  * fastgen_compact_plan + fastgen_compact (building K_C, V_C) and
- * fastgen_decode_attn (one generation step for every head).
+ * fastgen_decode_attn (one generation step for every head;
+ * fastgen_decode_attn_refresh also refreshes the frequent sets, an opt-in
+ * variant).
  *
  * Conventions shared by every entry point
  *   - Query heads are a flat index g = (b*L + l)*H + h over G = B*L*H
@@ -290,6 +292,61 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
                               const int32_t* punct_ids, int32_t n_punct, int32_t pos,
                               void* out, void* workspace, size_t workspace_bytes,
                               int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Decode-time refresh of C_frequent (opt-in variant; Method: C_frequent keeps
+ * the tokens with the largest cumulative attention scores, and the stability
+ * paragraph examines accumulated attention scores at the prompt and at later
+ * decoding steps).  The pages reuse the prompt-time policy and state no
+ * update rule; this variant is the library's own rule and is off unless
+ * these calls are used.
+ *
+ * Rule: every cached row j carries an accumulated score acc_j: its prompt
+ * column sum colsum_j at the end of the prompt (0 for a generated token when
+ * it is placed) plus, at every generation step, the attention weight the
+ * step's query gives it.  After every `period`-th step, a local-hybrid
+ * (FG_POLICY_SPFL) cache re-chooses its frequent members (the never-evicted
+ * rows kept for frequency, i.e. not special or punctuation tokens) as the
+ * |F| rows of largest acc among those members and the rows of the local
+ * window, ties to the lower position; |F| is fixed at the prompt, so the
+ * cache never grows.  A member that loses its place leaves the cache unless
+ * it is still inside the window (then it stays until it is w positions old);
+ * a window row that wins a place stays for good; dropped rows never return.
+ * Other policies have no window rows to promote and are left as profiled.
+ *
+ * Limits: no groups (Hkv == H, else FG_EINVAL); ceil(r_f n) + ceil(r_l n)
+ * <= 16384 (the candidates of one cache are ranked in shared memory, else
+ * FG_EINVAL).
+ *
+ * fastgen_refresh_state_bytes: size of the caller-owned state (per pool
+ *   row: acc float, the step's score float, a role byte), 256-byte aligned.
+ * fastgen_refresh_init: after fastgen_compact, sets acc from colsum [G, n]
+ *   (fastgen_profile's output) and marks the frequent slots from token_ids
+ *   [B, n] and the id sets.  Asynchronous on `stream`.
+ * fastgen_decode_attn_refresh: fastgen_decode_attn (same arguments and
+ *   outputs) that also accumulates every cached row's weight into acc and,
+ *   when (pos - n + 1) is a multiple of `period` (>= 1), runs the refresh
+ *   after the step.  With a period longer than the generation it gives
+ *   fastgen_decode_attn's outputs bit for bit.
+ * Errors: those of fastgen_decode_attn; FG_EINVAL for the limits above, a
+ * period < 1 or a NULL/misaligned state; FG_EWORKSPACE for a short state.
+ * ------------------------------------------------------------------------ */
+size_t fastgen_refresh_state_bytes(const fg_params* p, const fg_plan_info* info);
+
+fg_status fastgen_refresh_init(const fg_params* p, const void* plan, const fg_plan_info* info,
+                               const int32_t* pos_pool, const float* colsum,
+                               const int32_t* token_ids, const int32_t* special_ids,
+                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                               void* state, size_t state_bytes, void* stream);
+
+fg_status fastgen_decode_attn_refresh(const fg_params* p, void* plan, const fg_plan_info* info,
+                                      void* K_pool, void* V_pool, int32_t* pos_pool,
+                                      const void* q, const void* k_new, const void* v_new,
+                                      const int32_t* new_ids, const int32_t* special_ids,
+                                      int32_t n_special, const int32_t* punct_ids,
+                                      int32_t n_punct, int32_t pos, int32_t period, void* out,
+                                      void* state, size_t state_bytes, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * fastgen_decode_attn for callers that cannot allocate device memory.

@@ -204,3 +204,36 @@ def test_group_sizes_in_buffer_sizes():
     assert fg.fastgen_plan_bytes(p, 7) == al(Gkv * 40) + al(Gkv * 8) + 256 + work * 8
     info = fg.PlanInfo(1000, 13, 256)
     assert fg.fastgen_decode_workspace_bytes(p, info) == al(13 * 4 * 8) + al(13 * 4 * 128 * 4)
+
+
+def test_refresh_calls_reject_on_host():
+    """The refresh variant's limits and buffers are checked before any launch."""
+    L = fg.lib()
+    al = lambda x: (x + 255) // 256 * 256
+    p = P()
+    info = fg.PlanInfo(1000, 10, 256)
+    st = fg.fastgen_refresh_state_bytes(p, info)
+    assert st == 2 * al(1000 * 4) + al(1000)
+    ws = fg.fastgen_decode_workspace_bytes(p, info)
+
+    def dec(params=p, period=4, state=FAKE, state_bytes=st):
+        return L.fastgen_decode_attn_refresh(ctypes.byref(params), FAKE, ctypes.byref(info), FAKE,
+                                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1,
+                                             100, period, FAKE, state, state_bytes, FAKE, ws,
+                                             FAKE, None)
+
+    def init(params=p, state=FAKE, state_bytes=st, colsum=FAKE):
+        return L.fastgen_refresh_init(ctypes.byref(params), FAKE, ctypes.byref(info), FAKE, colsum,
+                                      FAKE, FAKE, 1, FAKE, 1, state, state_bytes, None)
+
+    assert dec(period=0) == fg.FG_EINVAL                      # period >= 1
+    assert dec(period=-3) == fg.FG_EINVAL
+    assert dec(params=P(H=4, Hkv=2)) == fg.FG_EINVAL          # groups are not supported
+    assert dec(params=P(n=20000, r_l=0.5, r_f=0.5)) == fg.FG_EINVAL  # k + w > 16384
+    assert dec(state=None) == fg.FG_EINVAL
+    assert dec(state=FAKE + 64) == fg.FG_EINVAL               # not 256-byte aligned
+    assert dec(state_bytes=st - 1) == fg.FG_EWORKSPACE
+    assert init(params=P(H=4, Hkv=2)) == fg.FG_EINVAL
+    assert init(state_bytes=st - 1) == fg.FG_EWORKSPACE
+    assert init(colsum=None) == fg.FG_EINVAL
+    assert init(params=P(T=0.0)) == fg.FG_EINVAL

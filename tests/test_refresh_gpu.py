@@ -1,0 +1,150 @@
+"""GPU parity of the opt-in refresh of C_frequent (fastgen_refresh_init +
+fastgen_decode_attn_refresh) against the oracle's decode_head_refresh, on the
+same seeded workloads as the main parity tests.
+
+Per head: the profile as in the main comparison (parity_util.compare), then
+every step's output, the final cache positions (after the last refresh) and
+the accumulated score of every cached row.  Tolerances are the main tests'
+(outputs 2e-2 for bf16, 1e-5 for fp32); accumulated scores within
+2e-4 |acc| + 1e-5 (the fp32 column sums they start from carry 1e-4 of the
+oracle's, plus fp32 weights).  A refresh whose oracle ranking has a near tie
+(the last member kept and the best candidate left out within 1e-4, relative)
+may go either way on the GPU: such a head is compared up to that step only.
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import CONFIGS
+
+pytestmark = pytest.mark.gpu
+
+NEAR_REFRESH = 1e-4
+ACC_RTOL, ACC_ATOL = 2e-4, 1e-5
+
+
+def run_refresh(cfg, period, seed=0):
+    from adaptive_head_kv_gb300.session import FastGenSession, make_params
+    from synth import make_workload, punct_ids, special_ids
+
+    w = make_workload(cfg, seed)
+    n, steps, dev = cfg.n, cfg.steps, torch.device("cuda")
+    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    s = FastGenSession(p, special_ids(seed), punct_ids(seed), steps, guard=True,
+                       refresh_period=period)
+    ids = torch.from_numpy(w["ids"]).to(dev)
+    s.prefill(w["Q"][:, :n].contiguous().to(dev), w["K"][:, :n].contiguous().to(dev),
+              w["V"][:, :n].contiguous().to(dev), ids[:, :n].contiguous())
+    outs = torch.empty(steps, s.G, cfg.d, dtype=s.tdtype, device=dev)
+    for st in range(steps):
+        t = n + st
+        s.decode(w["Q"][:, t].contiguous().to(dev), w["K"][:, t].contiguous().to(dev),
+                 w["V"][:, t].contiguous().to(dev), ids[:, t].contiguous(), t, out=outs[st])
+    torch.cuda.synchronize()
+    return dict(workload=w, session=s, policy=s.policy.cpu().numpy().astype(int),
+                keep=s.keep.cpu().numpy(), colsum=s.colsum.cpu().numpy().astype(np.float64),
+                out=outs.float().cpu().numpy().astype(np.float64), desc=s.descriptors(),
+                pos=s.pos_pool.cpu().numpy(), acc=s.row_scores().numpy().astype(np.float64),
+                dev_err=int(s.dev_err.item()), guards=s.check_guards())
+
+
+def cache_rows(desc, pos):
+    """(position, pool row) of every cached row of one cache."""
+    rows = [(int(pos[desc.off + r]), desc.off + r) for r in range(desc.n_static)]
+    rows += [(int(pos[desc.win_off + r]), desc.win_off + r) for r in range(desc.w)
+             if pos[desc.win_off + r] >= 0]
+    return sorted(rows)
+
+
+def compare_refresh(cfg, gpu, period):
+    from oracle import fastgen_oracle as O
+    from parity_util import dec_atol, policy_exempt, topk_exempt
+    from synth import punct_ids, special_ids
+
+    w = gpu["workload"]
+    T = float(np.float32(cfg.T))
+    n, steps = cfg.n, cfg.steps
+    rep = dict(heads=0, compared=0, refreshed_spfl=0, cut_short=0, promoted=0)
+    assert gpu["dev_err"] == 0 and gpu["guards"] == 0
+    for g in range(cfg.G):
+        b = g // (cfg.L * cfg.H)
+        Qa, Ka, Va = (w[x][g].double().numpy() for x in "QKV")
+        ids = w["ids"][b]
+        prof = O.profile_head(Qa[:n], Ka[:n], ids, special_ids(), punct_ids(), T, cfg.r_l,
+                              cfg.r_f)
+        rep["heads"] += 1
+        if policy_exempt(prof, T) or (topk_exempt(prof) and prof["policy"] in (2, 3)):
+            continue
+        assert gpu["policy"][g] == prof["policy"] and np.array_equal(gpu["keep"][g], prof["keep"])
+        r = O.decode_head_refresh(prof["policy"], prof["keep"], n, prof["w"], ids, Qa, Ka, Va,
+                                  special_ids(), punct_ids(), steps, prof["colsum"], period)
+        near = [i for i, gap in enumerate(r["gaps"]) if gap <= NEAR_REFRESH]
+        upto = steps if not near else (near[0] + 1) * period  # steps before the tie takes effect
+        err = np.abs(gpu["out"][:upto, g] - r["out"][:upto]).max() if upto else 0.0
+        assert err <= dec_atol(cfg.dtype), (g, err, prof["policy"])
+        rep["compared"] += 1
+        if near:
+            rep["cut_short"] += 1
+            continue
+        rows = cache_rows(gpu["desc"][g], gpu["pos"])
+        assert [p for p, _ in rows] == [int(x) for x in r["final"]], g
+        for p, row in rows:
+            want = r["acc"][p]
+            assert abs(gpu["acc"][row] - want) <= ACC_RTOL * abs(want) + ACC_ATOL, (g, p)
+        if prof["policy"] == O.P_SPFL and steps >= period:
+            rep["refreshed_spfl"] += 1
+            _, frozen = O.decode_head(prof["policy"], prof["keep"], n, prof["w"], ids, Qa, Ka,
+                                      Va, special_ids(), punct_ids(), steps)
+            rep["promoted"] += int(not np.array_equal(frozen, r["final"]))
+    return rep
+
+
+@pytest.mark.parametrize("name,kw,period", [
+    ("bf16_d128_p1", dict(dtype="bf16", d=128, L=2, H=6, n=300, steps=40, one_of_each=False), 1),
+    ("bf16_d128_p4", dict(dtype="bf16", d=128, L=2, H=6, n=300, steps=40, one_of_each=False), 4),
+    ("bf16_d64_p3", dict(dtype="bf16", d=64, L=2, H=4, n=257, steps=30), 3),
+    ("fp32_d128_p2", dict(dtype="fp32", d=128, L=1, H=8, n=200, steps=20, one_of_each=False), 2),
+    ("bf16_two_seqs_p5", dict(dtype="bf16", d=128, B=2, L=1, H=4, n=190, steps=25), 5),
+    ("window_tiny_p1", dict(dtype="bf16", d=128, r_l=0.01, n=150, steps=40), 1),
+])
+def test_refresh_small_shapes(name, kw, period):
+    cfg = CONFIGS["tiny"].with_(**kw)
+    rep = compare_refresh(cfg, run_refresh(cfg, period), period)
+    print(name, rep)
+    assert rep["compared"] >= rep["heads"] // 2, rep
+
+
+@pytest.mark.parametrize("base,kw,period", [
+    ("llama7b", dict(L=2, H=8, steps=64), 8),
+    ("long8k", dict(L=1, H=4, steps=32), 16),
+])
+def test_refresh_config_shapes(base, kw, period):
+    """Full prompt lengths and head dims of the configs, fewer heads."""
+    cfg = CONFIGS[base].with_(**kw)
+    rep = compare_refresh(cfg, run_refresh(cfg, period), period)
+    print(base, rep)
+    assert rep["compared"] >= rep["heads"] // 2, rep
+    assert rep["refreshed_spfl"] >= 1, rep
+
+
+def test_refresh_changes_caches_somewhere():
+    """The rule is not vacuous on the synthetic workload: some local-hybrid
+    cache ends with a different membership than the frozen path."""
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=4, H=8, n=300, steps=48,
+                                one_of_each=False)
+    rep = compare_refresh(cfg, run_refresh(cfg, 1), 1)
+    print(rep)
+    assert rep["promoted"] >= 1, rep
+
+
+def test_period_beyond_generation_is_the_plain_decode_bit_for_bit():
+    """With no refresh reached, the refresh call gives fastgen_decode_attn's
+    outputs and caches exactly (it only adds the score bookkeeping)."""
+    from parity_util import run_gpu
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=6, n=300, steps=24,
+                                one_of_each=False)
+    ref = run_gpu(cfg)
+    got = run_refresh(cfg, cfg.steps + 1)
+    assert np.array_equal(got["out"], ref["out"])
+    assert np.array_equal(got["pos"], ref["pos1"])
