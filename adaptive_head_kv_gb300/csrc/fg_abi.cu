@@ -110,7 +110,8 @@ static fg_status profile_call(const fg_params* p, const void* Q, const void* K, 
                               int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
                               const int8_t* fixed, int8_t* policy, float* mass, int32_t* cost,
                               float* colsum, uint8_t* keep, int32_t* kept, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_err, void* stream) {
+                              size_t workspace_bytes, int32_t* dev_err, void* stream,
+                              int stall_pass = 0) {
   fg_status st = check_params(p);
   if (st != FG_OK) return st;
   if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
@@ -147,7 +148,7 @@ static fg_status profile_call(const fg_params* p, const void* Q, const void* K, 
   if (e == cudaSuccess) {
     if (tc)
       e = fg::launch_profile_tc(pd, Q, K, lse2, ld, colsum, bandcol, fixed ? heads : nullptr,
-                                fixed ? sched + 2 : nullptr, sched, dev_err, s);
+                                fixed ? sched + 2 : nullptr, sched, dev_err, stall_pass, s);
     else  // the fp32 path scores every head
       e = fg::launch_profile_simt(pd, Q, K, lse2, ld, colsum, bandcol, s);
   }
@@ -193,6 +194,20 @@ fg_status fastgen_profile_with_policy(const fg_params* p, const void* Q, const v
   return profile_call(p, Q, K, nullptr, nullptr, token_ids, special_ids, n_special, punct_ids,
                       n_punct, policy, nullptr, nullptr, nullptr, colsum, keep, kept, workspace,
                       workspace_bytes, dev_err, stream);
+}
+
+fg_status fastgen_profile_stall_test(const fg_params* p, const void* Q, const void* K,
+                                     const int32_t* token_ids, const int32_t* special_ids,
+                                     int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                                     int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                                     uint8_t* keep, int32_t* kept, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err, int32_t stall_pass,
+                                     void* stream) {
+  if (stall_pass != 1 && stall_pass != 2) return FG_EINVAL;
+  if (!p || p->dtype != FG_BF16) return FG_EDTYPE;  // the bounded waits are the tensor-core passes'
+  return profile_call(p, Q, K, nullptr, nullptr, token_ids, special_ids, n_special, punct_ids,
+                      n_punct, nullptr, policy, mass, cost, colsum, keep, kept, workspace,
+                      workspace_bytes, dev_err, stream, stall_pass);
 }
 
 size_t fastgen_plan_bytes(const fg_params* p, int32_t max_new_tokens) {

@@ -41,11 +41,13 @@ cudaError_t launch_profile_simt(const ProfileDims& pd, const void* Q, const void
 // heads / n_heads (device): when heads is non-null only the *n_heads listed
 // heads are profiled.  sched: two ints of scratch (the passes' work
 // counters).  A device-side wait that times out ORs 2 into *err.
+// stall_pass (1 or 2; 0 in normal use) keeps that pass's producer from
+// starting, so its waits run out: a test of the error path.
 bool profile_tc_supported(const ProfileDims& pd);
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
                               int ld, float* colsum, float* bandcol, const int32_t* heads,
                               const int32_t* n_heads, int32_t* sched, int32_t* err,
-                              cudaStream_t s);
+                              int stall_pass, cudaStream_t s);
 
 // Pass 3: the prompt attention output out [G, n, d] = A V, from pass 1's
 // negated base-2 row LSEs.  bf16 on the tensor cores (sched: one zeroed work

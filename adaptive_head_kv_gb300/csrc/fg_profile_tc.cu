@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                       float* __restrict__ colsum, float* __restrict__ bandcol, int G, int n,
                       int ld, int nt, int w, float sl2, int H, int R,
                       const int32_t* __restrict__ heads, const int32_t* __restrict__ n_heads,
-                      int32_t* __restrict__ sched, int32_t* __restrict__ err) {
+                      int32_t* __restrict__ sched, int32_t* __restrict__ err, int stall) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& s = *reinterpret_cast<TcSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -281,7 +281,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- producer (TMA)
-    if (lane == 0) {
+    // stall != 0 (a test of the error path only): the producer never starts,
+    // so the other warps' first waits run out and the CTA unwinds with
+    // nothing in flight
+    if (lane == 0 && !stall) {
       // every head, or the listed ones (a saved policy map)
       const int total_units = (heads ? *n_heads : G) * nt;
       int bseq = 0, lseq = 0, ucount = 0;
@@ -940,7 +943,7 @@ int sm_count() {
 template <int D>
 cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse2, int ld,
                 float* colsum, float* bandcol, const int32_t* heads, const int32_t* n_heads,
-                int32_t* sched, int32_t* err, cudaStream_t s) {
+                int32_t* sched, int32_t* err, int stall_pass, cudaStream_t s) {
   CUtensorMap tq, tk;
   if (!make_map(&tq, Q, pd.G, pd.n, D) || !make_map(&tk, K, pd.Gkv, pd.n, D))
     return cudaErrorInvalidValue;
@@ -958,11 +961,12 @@ cudaError_t run(const ProfileDims& pd, const void* Q, const void* K, float* nlse
   const unsigned grid = (unsigned)(units < 2LL * sms ? units : 2LL * sms);
   // the work counters were zeroed by the token-class kernel launched before
   e = launch_pdl(profile_tc_kernel<1, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum, bandcol,
-                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, heads, n_heads, sched, err);
+                 pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, heads, n_heads, sched, err,
+                 (int)(stall_pass == 1));
   if (e == cudaSuccess)
     e = launch_pdl(profile_tc_kernel<2, D>, grid, kThreads, smem, s, tq, tk, nlse2, colsum,
                    bandcol, pd.G, pd.n, ld, nt, pd.w, pd.sl2, pd.H, pd.R, heads, n_heads,
-                   sched + 1, err);
+                   sched + 1, err, (int)(stall_pass == 2));
   return e;
 }
 
@@ -997,10 +1001,11 @@ bool profile_tc_supported(const ProfileDims& pd) {
 cudaError_t launch_profile_tc(const ProfileDims& pd, const void* Q, const void* K, float* lse2,
                               int ld, float* colsum, float* bandcol, const int32_t* heads,
                               const int32_t* n_heads, int32_t* sched, int32_t* err,
-                              cudaStream_t s) {
-  return pd.d == 64
-             ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s)
-             : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err, s);
+                              int stall_pass, cudaStream_t s) {
+  return pd.d == 64 ? run<64>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err,
+                              stall_pass, s)
+                    : run<128>(pd, Q, K, lse2, ld, colsum, bandcol, heads, n_heads, sched, err,
+                               stall_pass, s);
 }
 
 cudaError_t launch_attn_tc(const ProfileDims& pd, const void* Q, const void* K, const void* V,

@@ -31,7 +31,7 @@ EXPORTS = (
     "fastgen_decode_workspace_bytes", "fastgen_decode_attn", "fastgen_read_error",
     "fastgen_decode_attn_noalloc", "fastgen_profile_with_policy", "fastgen_profile_attn",
     "fastgen_plan_compact", "fastgen_refresh_state_bytes", "fastgen_refresh_init",
-    "fastgen_decode_attn_refresh",
+    "fastgen_decode_attn_refresh", "fastgen_profile_stall_test",
 )
 
 # size of the library-held scratch array used by fastgen_decode_attn_noalloc
@@ -89,6 +89,9 @@ _SIGS = {
                                            _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                            _P, _P, _SZ, _P, _P]),
     "fastgen_read_error": (ctypes.c_int, [_P, _P]),
+    "fastgen_profile_stall_test": (ctypes.c_int, [ctypes.POINTER(Params), _P, _P, _P, _P, _I32,
+                                                  _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                                  _I32, _P]),
     "fastgen_refresh_state_bytes": (_SZ, [ctypes.POINTER(Params), ctypes.POINTER(PlanInfo)]),
     "fastgen_refresh_init": (ctypes.c_int, [ctypes.POINTER(Params), _P, ctypes.POINTER(PlanInfo),
                                             _P, _P, _P, _P, _I32, _P, _I32, _P, _SZ, _P]),
@@ -281,3 +284,15 @@ def fastgen_decode_attn_refresh(params, plan, info, K_pool, V_pool, pos_pool, q,
         _count(special_ids), _ptr(punct_ids), _count(punct_ids), int(pos), int(period),
         _ptr(out), _ptr(state), _nbytes(state), _ptr(workspace), _nbytes(workspace),
         _ptr(dev_err), _stream(stream)), "fastgen_decode_attn_refresh")
+
+
+def fastgen_profile_stall_test(params, Q, K, token_ids, special_ids, punct_ids, policy, mass,
+                               cost, colsum, keep, kept, workspace, dev_err, stall_pass,
+                               stream=None) -> None:
+    """fastgen_profile with one tensor-core pass's producer held back, so
+    that pass's bounded waits run out (a test of the error path)."""
+    _check(lib().fastgen_profile_stall_test(
+        ctypes.byref(params), _ptr(Q), _ptr(K), _ptr(token_ids), _ptr(special_ids),
+        _count(special_ids), _ptr(punct_ids), _count(punct_ids), _ptr(policy), _ptr(mass),
+        _ptr(cost), _ptr(colsum), _ptr(keep), _ptr(kept), _ptr(workspace), _nbytes(workspace),
+        _ptr(dev_err), int(stall_pass), _stream(stream)), "fastgen_profile_stall_test")

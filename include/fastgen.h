@@ -396,6 +396,26 @@ fg_status fastgen_decode_attn_noalloc(const fg_params* p, void* plan, const fg_p
                                       int32_t n_punct, int32_t pos, void* out,
                                       int32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Test support for the bounded-wait error path (the paper has no
+ * counterpart).  fastgen_profile, except that the producer warp of tensor-core
+ * pass `stall_pass` (1: row log-sum-exps, 2: column sums) never starts: the
+ * pass's other warps wait for work that never comes, each wait runs out after
+ * its limit (about 1 s), and every CTA unwinds with no copy or MMA in flight
+ * and ORs 2 into *dev_err (fastgen_read_error then gives FG_EDEVICE).  The
+ * stalled pass's outputs are left as they were; the context stays usable and
+ * later calls on the stream run normally.  bf16 inputs only (FG_EDTYPE
+ * otherwise); FG_EINVAL for another stall_pass; other errors as
+ * fastgen_profile.
+ * ------------------------------------------------------------------------ */
+fg_status fastgen_profile_stall_test(const fg_params* p, const void* Q, const void* K,
+                                     const int32_t* token_ids, const int32_t* special_ids,
+                                     int32_t n_special, const int32_t* punct_ids, int32_t n_punct,
+                                     int8_t* policy, float* mass, int32_t* cost, float* colsum,
+                                     uint8_t* keep, int32_t* kept, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err, int32_t stall_pass,
+                                     void* stream);
+
 /* Synchronously reads a device flag written by fastgen_profile,
  * fastgen_profile_with_policy or fastgen_decode_attn and maps it to a status
  * (FG_OK, FG_ECAPACITY, FG_EINVAL for an out-of-range saved policy, or

@@ -237,3 +237,17 @@ def test_refresh_calls_reject_on_host():
     assert init(state_bytes=st - 1) == fg.FG_EWORKSPACE
     assert init(colsum=None) == fg.FG_EINVAL
     assert init(params=P(T=0.0)) == fg.FG_EINVAL
+
+
+def test_stall_test_rejects_on_host():
+    L = fg.lib()
+
+    def call(stall=1, **kw):
+        return L.fastgen_profile_stall_test(ctypes.byref(P(**kw)), FAKE, FAKE, FAKE, FAKE, 1, FAKE,
+                                            1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
+                                            FAKE, stall, None)
+
+    assert call(stall=0) == fg.FG_EINVAL
+    assert call(stall=3) == fg.FG_EINVAL
+    assert call(dtype=fg.FG_FP32) == fg.FG_EDTYPE
+    assert call(T=0.0) == fg.FG_EINVAL

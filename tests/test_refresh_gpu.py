@@ -116,7 +116,7 @@ def test_refresh_small_shapes(name, kw, period):
 
 @pytest.mark.parametrize("base,kw,period", [
     ("llama7b", dict(L=2, H=8, steps=64), 8),
-    ("long8k", dict(L=1, H=4, steps=32), 16),
+    ("long8k", dict(L=1, H=8, steps=32, one_of_each=True), 16),  # heads 2, 6 local
 ])
 def test_refresh_config_shapes(base, kw, period):
     """Full prompt lengths and head dims of the configs, fewer heads."""
