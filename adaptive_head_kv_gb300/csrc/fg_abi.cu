@@ -231,17 +231,25 @@ fg_status fastgen_compact_plan(const fg_params* p, const int8_t* policy, const u
   long long* totals = (long long*)(base + plan_desc_bytes(pd.Gkv) + plan_cinfo_bytes(pd.Gkv));
   int2* work = (int2*)(base + plan_work_offset(pd.Gkv));
   cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FG_ECUDA;
+  // wide items once there are 64 small ones per SM (16 waves of 4 CTAs)
+  const int wide_at = 64 * sms;
   cudaError_t e = fg::launch_group(pd, policy, keep, cinfo, s);
   if (e == cudaSuccess)
-    e = fg::launch_plan(pd.Gkv, pd.w, max_new_tokens, cinfo, desc, work, totals, s);
-  long long h[2] = {0, 0};
+    e = fg::launch_plan(pd.Gkv, pd.w, max_new_tokens, wide_at, cinfo, desc, work, totals, s);
+  long long h[3] = {0, 0, 0};
   if (e == cudaSuccess) e = cudaMemcpyAsync(h, totals, sizeof(h), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return FG_ECUDA;
-  if (h[1] > (long long)plan_max_work(p, max_new_tokens) || h[1] > 0x7fffffffLL) return FG_ECUDA;
+  if (h[1] > (long long)plan_max_work(p, max_new_tokens) || h[1] > 0x7fffffffLL ||
+      (h[2] != fg::kRowsPerWork && h[2] != fg::kRowsPerWorkWide))
+    return FG_ECUDA;
   info->pool_rows = h[0];
   info->n_work = (int32_t)h[1];
-  info->rows_per_work = fg::kRowsPerWork;
+  info->rows_per_work = (int32_t)h[2];
   return FG_OK;
 }
 
@@ -301,10 +309,13 @@ static fg_status decode_call(const fg_params* p, void* plan, const fg_plan_info*
       !aligned(workspace, kAlign) || !aligned(dev_err, 4) || !aligned(pos_pool, 4))
     return FG_EINVAL;
   if (pos < p->n || info->n_work < 0) return FG_EINVAL;
+  if (info->rows_per_work != fg::kRowsPerWork && info->rows_per_work != fg::kRowsPerWorkWide)
+    return FG_EINVAL;
   if (workspace_bytes < fastgen_decode_workspace_bytes(p, info)) return FG_EWORKSPACE;
   const fg::ProfileDims pd = dims(p);
   char* base = (char*)plan;
   fg::DecodeArgs a;
+  a.rpw = info->rows_per_work;
   a.desc = (fg_head_desc*)base;
   a.work = (const int2*)(base + plan_work_offset(pd.Gkv));
   a.n_work = info->n_work;

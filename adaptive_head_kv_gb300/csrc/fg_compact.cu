@@ -9,7 +9,9 @@
 //                                  of position t at slot t mod w.
 // One cache per key/value head holds the union of its query heads' caches.
 // The plan kernel lays caches out by an exclusive scan of their row counts
-// and also emits the decode work list (one item per kRowsPerWork rows).
+// and also emits the decode work list (one item per kRowsPerWork rows of the
+// prompt's never-evicted rows, the last one also taking the rows appended
+// while generating, plus one per kRowsPerWork rows of the ring).
 #include "fg_common.cuh"
 #include "fg_internal.h"
 
@@ -56,11 +58,34 @@ __global__ void __launch_bounds__(256) group_kernel(const int8_t* __restrict__ p
   }
 }
 
+// Decode work items of a cache at `rpw` rows per item: the never-evicted
+// segment's prompt rows (at least one item; the last one also takes the rows
+// appended later) and the window ring.
+__device__ __forceinline__ int cache_items(int n_static, int wg, int rpw) {
+  return max(1, cdiv(n_static, rpw)) + cdiv(wg, rpw);
+}
+
+// Item size: kRowsPerWork, or kRowsPerWorkWide when the plan would have at
+// least `wide_at` items at the small size (plenty of CTAs either way; the
+// wide items halve the fixed cost per item).
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
-    const int2* __restrict__ cinfo, int G, int w, int reserve, fg_head_desc* __restrict__ desc,
-    long long* __restrict__ totals) {
+    const int2* __restrict__ cinfo, int G, int w, int reserve, int wide_at,
+    fg_head_desc* __restrict__ desc, long long* __restrict__ totals) {
   __shared__ long long scr64[33];
   __shared__ int scr32[33];
+  int small_items = 0;
+  for (int base = 0; base < G; base += blockDim.x) {
+    const int g = base + threadIdx.x;
+    int works = 0;
+    if (g < G) {
+      const int2 ci = cinfo[g];
+      works = cache_items(ci.y, ci.x == FG_POLICY_SPFL ? w : 0, kRowsPerWork);
+    }
+    int wtot;
+    block_exclusive_scan(works, scr32, &wtot);
+    small_items += wtot;
+  }
+  const int rpw = small_items >= wide_at ? kRowsPerWorkWide : kRowsPerWork;
   long long row_base = 0;
   int work_base = 0;
   for (int base = 0; base < G; base += blockDim.x) {
@@ -74,7 +99,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
       cap = n_static + reserve;
       wg = (p == FG_POLICY_SPFL) ? w : 0;
       rows = (long long)cap + wg;
-      works = max(1, cdiv(cap, kRowsPerWork) + cdiv(wg, kRowsPerWork));
+      works = cache_items(n_static, wg, rpw);
     }
     long long rtot;
     int wtot;
@@ -98,6 +123,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
   if (threadIdx.x == 0) {
     totals[0] = row_base;
     totals[1] = work_base;
+    totals[2] = rpw;
   }
 }
 
@@ -195,9 +221,9 @@ cudaError_t launch_group(const ProfileDims& pd, const int8_t* policy, const uint
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(int Gkv, int w, int reserve, const int2* cinfo, fg_head_desc* desc,
-                        int2* work, long long* totals, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(cinfo, Gkv, w, reserve, desc, totals);
+cudaError_t launch_plan(int Gkv, int w, int reserve, int wide_at, const int2* cinfo,
+                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(cinfo, Gkv, w, reserve, wide_at, desc, totals);
   worklist_kernel<<<cdiv(Gkv, 256), 256, 0, s>>>(desc, Gkv, work);
   return cudaGetLastError();
 }

@@ -2,9 +2,12 @@
 // What to Discard, Method: head-specific KV caches, keys/values appended at
 // each step, the prompt-time policy reused during generation).
 //
-// Split-K over a static work list: item (c, i) covers up to kRowsPerWork
-// rows of cache c's never-evicted segment or of its window ring (one cache
-// per key/value head; its R query heads all attend over it).  Each CTA
+// Split-K over a static work list: item (c, i) covers rpw rows (256, or 512
+// in plans with many items) of
+// cache c's never-evicted segment or of its window ring (one cache per
+// key/value head; its R query heads all attend over it).  The segment's last
+// item also covers every row appended after the prompt, so no item is spent
+// on the reserve that is still empty.  Each CTA
 //   * places the new token if its slot falls in the item (the only writer of
 //     that row; it attends with the new key/value from registers, so no CTA
 //     reads a row written in this launch),
@@ -69,19 +72,21 @@ __device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi
   int chunk = it.y;
   const fg_head_desc hd = a.desc[m.c];
   const Placement pl = place(hd, a, HLkv, m.c);
-  const int nsc = cdiv(hd.static_cap, kRowsPerWork);
+  const int rpw = a.rpw;
+  const int nsc = hd.n_work - cdiv(hd.w, rpw);  // items of the never-evicted segment
   m.ring = chunk >= nsc;
   m.evict = -1;
   if (!m.ring) {
-    m.r0 = chunk * kRowsPerWork;
-    m.r1 = min(m.r0 + kRowsPerWork, hd.n_static + (pl.st ? 1 : 0));
+    const int rows = hd.n_static + (pl.st ? 1 : 0);
+    m.r0 = chunk * rpw;
+    m.r1 = chunk == nsc - 1 ? rows : min(m.r0 + rpw, rows);
     m.base = hd.off;
     m.new_slot = pl.st ? hd.n_static : -1;
     if (pl.overflow && chunk == 0 && threadIdx.x == 0) atomicOr(a.dev_err, 1);
   } else {
     chunk -= nsc;
-    m.r0 = chunk * kRowsPerWork;
-    m.r1 = min(m.r0 + kRowsPerWork, hd.w);
+    m.r0 = chunk * rpw;
+    m.r1 = min(m.r0 + rpw, hd.w);
     m.base = hd.win_off;
     const int slot = a.pos % hd.w;
     m.new_slot = pl.ring_put ? slot : -1;
@@ -314,9 +319,8 @@ __global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, 
 constexpr int kMmaWarps = 4;
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaBlk = 16;                                   // rows per MMA tile
-constexpr int kMmaNB = kRowsPerWork / (kMmaWarps * kMmaBlk);  // blocks per warp
 constexpr int kMmaStages = 2;                                 // V blocks in flight per warp
-static_assert(kMmaNB * kMmaWarps * kMmaBlk == kRowsPerWork, "item = whole blocks");
+static_assert(kRowsPerWork % (kMmaWarps * kMmaBlk) == 0, "items are whole blocks");
 
 template <int D>
 struct MmaSmem {
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeA
   // requested before this block's scores.
   const int first = it.r0 + warp * kMmaBlk;
   const int nblk =
-      first < it.r1 ? min(kMmaNB, cdiv(it.r1 - first, kMmaWarps * kMmaBlk)) : 0;
+      first < it.r1 ? cdiv(it.r1 - first, kMmaWarps * kMmaBlk) : 0;
   const uint32_t vring =
       smem_u32(mma_smem) + (uint32_t)(warp * kMmaStages * SM::kStageElems * 2);
   // K: rows g and g + 8 of a block, pieces {32 i + 8 t4}; k-step 2i + h takes

@@ -8,8 +8,12 @@
 
 namespace fg {
 
-// Decode work item: up to kRowsPerWork consecutive cache rows of one head.
+// Decode work item: kRowsPerWork (or, in plans with many items,
+// kRowsPerWorkWide) consecutive cache rows of one head; the last item of a
+// never-evicted segment also covers the rows appended later.  Buffer sizes
+// are bounded with kRowsPerWork, the smaller size.
 constexpr int kRowsPerWork = 256;
+constexpr int kRowsPerWorkWide = 512;
 
 struct ProfileDims {
   int G, HL, B, n, d, dtype;
@@ -77,8 +81,10 @@ cudaError_t launch_group(const ProfileDims& pd, const int8_t* policy, const uint
 
 // Writes one descriptor per cache from cinfo and builds the decode work list
 // (every cache gets at least one item).
-cudaError_t launch_plan(int Gkv, int w, int reserve, const int2* cinfo, fg_head_desc* desc,
-                        int2* work, long long* totals, cudaStream_t s);
+// Item size: kRowsPerWorkWide when the plan has >= wide_at items at
+// kRowsPerWork; totals = {pool rows, items, rows per item}.
+cudaError_t launch_plan(int Gkv, int w, int reserve, int wide_at, const int2* cinfo,
+                        fg_head_desc* desc, int2* work, long long* totals, cudaStream_t s);
 
 cudaError_t launch_compact(const ProfileDims& pd, const void* K, const void* V,
                            const uint8_t* keep, const fg_head_desc* desc, void* Kp, void* Vp,
@@ -100,6 +106,7 @@ struct DecodeArgs {
   const int32_t* punct;
   int np;
   int pos;
+  int rpw;  // rows per work item of the plan
   void* out;
   float* part_ml;   // [n_work, R, 2]
   float* part_acc;  // [n_work, R, d]

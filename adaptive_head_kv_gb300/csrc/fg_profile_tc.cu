@@ -155,12 +155,14 @@ __device__ __forceinline__ void lse_tile(uint32_t (&r)[2][32], float sl2, int c0
 
 // Pass 2, one thread's NC x 32 columns (starting at tile column c0) of a key row:
 // adds sum A to cs and the part inside the band to bs.  Called by all lanes of
-// a warp together.  nl = negated base-2
-// LSEs of the tile's 128 queries (-inf past the prompt end).  Tile columns
+// a warp together.  Lv = the negated base-2 LSEs of those NC x 32 queries
+// (-inf past the prompt end), four per vector, loaded before the scores so
+// that the shared-memory reads overlap the tensor-memory load.  Tile columns
 // c < lo precede the key (masked); columns c < band lie in the window.
 template <int NC>
-__device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const float* nl, float sl2,
-                                         int c0, int lo, int band, float& cs, float& bs) {
+__device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const float4 (&Lv)[8 * NC],
+                                         float sl2, int c0, int lo, int band, float& cs,
+                                         float& bs) {
   constexpr int kCols = NC * 32;
   const uint64_t s2 = pack2(sl2, sl2);
   // no lane of the warp needs a per-element test: one packed path
@@ -170,7 +172,7 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
     for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        const float4 L = *reinterpret_cast<const float4*>(nl + c0 + c * 32 + e);
+        const float4 L = Lv[c * 8 + e / 4];
         float x0, x1, x2, x3;
         unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
         unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
@@ -200,7 +202,7 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
       const int col = c0 + c * 32 + e;
-      const float4 L = *reinterpret_cast<const float4*>(nl + col);
+      const float4 L = Lv[c * 8 + e / 4];
       float x0, x1, x2, x3;
       unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
       unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
@@ -442,16 +444,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           // window for i < self + w; the row is read in two halves of 32
           // columns to keep the register pressure low
           uint32_t r[1][32];
+          float4 Lv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            Lv[e] = *reinterpret_cast<const float4*>(s.nlse[ls] + c0 + 4 * e);
           tmem_ld32(lane_base + buf * kBlk, r[0]);
           tmem_wait_ld(r[0]);
-          col_tile<1>(r, s.nlse[ls], sl2, c0, self - other0, self + w - other0, cs, bs);
+          col_tile<1>(r, Lv, sl2, c0, self - other0, self + w - other0, cs, bs);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            Lv[e] = *reinterpret_cast<const float4*>(s.nlse[ls] + c0 + 32 + 4 * e);
           tmem_ld32(lane_base + buf * kBlk + 32, r[0]);
           tmem_wait_ld(r[0]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s.sempty[buf]);
           ++sseq;
-          col_tile<1>(r, s.nlse[ls], sl2, c0 + 32, self - other0, self + w - other0, cs, bs);
+          col_tile<1>(r, Lv, sl2, c0 + 32, self - other0, self + w - other0, cs, bs);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s.lempty[ls]);
           ++lseq;

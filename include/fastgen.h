@@ -104,7 +104,8 @@ typedef struct {
 typedef struct {
   int64_t pool_rows;     /* rows the K, V and position pools must hold */
   int32_t n_work;        /* decode work items of the plan */
-  int32_t rows_per_work; /* cache rows covered by one decode work item */
+  int32_t rows_per_work; /* cache rows covered by one decode work item (the last item of a
+                            never-evicted segment also covers the rows appended later) */
 } fg_plan_info;
 
 /* Human-readable text of a status code (static storage). */
@@ -380,9 +381,9 @@ fg_status fastgen_decode_attn_refresh(const fg_params* p, void* plan, const fg_p
  *     <= FASTGEN_NOALLOC_SCRATCH_BYTES, i.e. roughly
  *     info->n_work * (H / Hkv) * (d + 2) * 4 bytes <= 8 MiB: about 16,000
  *     work items at d = 128 without groups, 8,000 with groups of 2, 2,000
- *     with groups of 8 (one work item covers up to info->rows_per_work = 256
+ *     with groups of 8 (one work item covers info->rows_per_work = 256 or 512
  *     rows of one cache).  The 7B attention shape (1024 heads, 2048-token
- *     prompt, 256 new tokens: about 5,600 items) fits; the 13B, 65B and
+ *     prompt, 256 new tokens: about 5,000 items) fits; the 13B, 65B and
  *     long-prompt shapes do not.  Larger plans return FG_EWORKSPACE before
  *     anything is launched; other errors as fastgen_decode_attn.
  * ------------------------------------------------------------------------ */

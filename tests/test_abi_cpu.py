@@ -181,6 +181,10 @@ def test_plan_compact_decode_reject_on_host():
                                      ws_bytes, FAKE, None)
 
     assert dec(pos=99) == fg.FG_EINVAL                 # a generated position precedes the prompt end
+    odd = fg.PlanInfo(500, 10, 300)                    # rows per item other than 256 or 512
+    assert L.fastgen_decode_attn(ctypes.byref(p), FAKE, ctypes.byref(odd), FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 100, FAKE, FAKE, ws, FAKE,
+                                 None) == fg.FG_EINVAL
     assert dec(ws_bytes=ws - 1) == fg.FG_EWORKSPACE
     assert dec(q=FAKE + 4) == fg.FG_EINVAL
     assert L.fastgen_read_error(None, None) == fg.FG_EINVAL

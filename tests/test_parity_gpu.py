@@ -95,6 +95,7 @@ def test_llama7b_full_size_sampled():
     heads against the oracle (all decode steps)."""
     cfg = CONFIGS["llama7b"]
     gpu = run_gpu(cfg, check_pools=True)
+    assert gpu["info"].rows_per_work == 256  # about 5,000 items: the small size
     heads = sample_heads(cfg, head_types(cfg), 24)
     rep = compare(cfg, gpu, heads)
     assert gpu["dev_err"] == 0
@@ -205,7 +206,8 @@ def run_full_size(cfg):
                mass=s.mass.cpu().numpy().astype(np.float64), cost=s.cost.cpu().numpy(),
                colsum=s.colsum.cpu().numpy().astype(np.float64), keep=s.keep.cpu().numpy(),
                kept=s.kept.cpu().numpy(), out=_HeadColumns(outs), desc1=s.descriptors(),
-               pos1=s.pos_pool.cpu().numpy(), dev_err=int(s.dev_err.item()))
+               pos1=s.pos_pool.cpu().numpy(), dev_err=int(s.dev_err.item()),
+               rows_per_work=int(s.info.rows_per_work))
     return gpu, w["types"]
 
 
@@ -220,6 +222,7 @@ def test_llama65b_full_size_sampled():
     cfg = CONFIGS["llama65b"]
     gpu, types = run_full_size(cfg)
     assert gpu["dev_err"] == 0
+    assert gpu["rows_per_work"] == 512  # a plan with many items takes the wide items
     heads = sample_heads(cfg, types, 16)
     gpu["workload"] = make_workload(cfg, heads=heads)
     rep = compare(cfg, gpu, range(len(heads)))
