@@ -53,10 +53,13 @@ def source_digest(group):
     return h.hexdigest()
 
 
-def record_traffic(csv_path, workload, command):
+def record_traffic(csv_path, workload, command, scale=None, measured_on=None):
     """Writes DRAM bytes per call of each kernel group from an ncu CSV (metrics
     dram__bytes_read.sum and dram__bytes_write.sum), tagged with the sources'
-    digest so that a later kernel change voids the figure."""
+    digest so that a later kernel change voids the figure.  With `scale`
+    ({group: factor}), the figures were captured on the smaller workload
+    `measured_on` and are scaled to `workload` by the ratio of the units
+    each call processes (recorded with the figure)."""
     import csv
 
     rows = list(csv.reader(open(csv_path)))
@@ -64,21 +67,32 @@ def record_traffic(csv_path, workload, command):
     h = rows[hi]
     ki, mi, vi, ui = (h.index(x) for x in ("Kernel Name", "Metric Name", "Metric Value",
                                             "Metric Unit"))
-    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    unit = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     out = {}
+    try:  # figures of other groups recorded earlier stay
+        with open(TRAFFIC_FILE) as f:
+            out = json.load(f)
+    except (OSError, ValueError):
+        out = {}
     for group, spec in KERNEL_GROUPS.items():
+        if scale and group not in scale:
+            continue
         total, calls = 0.0, 0
         for r in rows[hi + 1:]:
             if len(r) != len(h) or not any(p in r[ki] for p in spec["patterns"]):
                 continue
             if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-                total += float(r[vi].replace(",", "")) * scale[r[ui]]
+                total += float(r[vi].replace(",", "")) * unit[r[ui]]
             if r[mi] == "dram__bytes_read.sum" and spec["calls"] in r[ki]:
                 calls += 1
         if calls:
-            out[group] = {"bytes_per_call": total / calls, "calls": calls,
+            f = (scale or {}).get(group, 1.0)
+            out[group] = {"bytes_per_call": total / calls * f, "calls": calls,
                           "workload": workload, "source_sha256": source_digest(group),
                           "command": command}
+            if scale:
+                out[group].update(measured_on=measured_on, measured_bytes_per_call=total / calls,
+                                  scale=f)
     os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
     with open(TRAFFIC_FILE, "w") as f:
         json.dump(out, f, indent=1)
@@ -545,6 +559,11 @@ def main():
                     help="write profiles/traffic.json from an ncu CSV of DRAM byte counters")
     ap.add_argument("--traffic-command", default="",
                     help="the command that produced the CSV (stored with the figures)")
+    ap.add_argument("--traffic-scale", default="",
+                    help="group=factor,...: the CSV was captured on a smaller case of the "
+                         "workload; scale each group's bytes by the ratio of units per call")
+    ap.add_argument("--traffic-measured-on", default="",
+                    help="the smaller workload the scaled CSV was captured on")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -558,7 +577,10 @@ def main():
     if args.hkv:
         cfg = cfg.with_(Hkv=args.hkv, name=f"{cfg.name}_kv{args.hkv}")
     if args.record_traffic:
-        record_traffic(args.record_traffic, cfg.name, args.traffic_command)
+        scale = {k: float(v) for k, v in (x.split("=") for x in args.traffic_scale.split(",")
+                                          if x)} or None
+        record_traffic(args.record_traffic, cfg.name, args.traffic_command, scale,
+                       args.traffic_measured_on or None)
         return
     if args.impl == "reference":
         if rank != 0:
