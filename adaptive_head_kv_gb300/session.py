@@ -134,27 +134,28 @@ class FastGenSession:
         self.compact(K, V)
 
     def prefill_host(self, hQ, hK, hV, htoken_ids, Q, K, V, token_ids):
-        """prefill() from pinned host tensors: each of Q, K, V (and the ids)
-        is copied into its device buffer on its own stream, so the copies run
-        concurrently and the V copy overlaps the profiling."""
+        """prefill() from pinned host tensors: Q (with the ids), K and V are
+        copied in that order on one copy stream, and profiling starts as soon
+        as Q and K are on the device, so the V copy overlaps it.  One copy at
+        a time keeps the host link at its full rate: on the GB300 machines used,
+        three concurrent 21 GB copies shared about half of it (103 GB/s in
+        all against 211 GB/s for one)."""
         main = torch.cuda.current_stream(self.device)
-        if not hasattr(self, "_copy_streams"):
-            self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(3)]
-        done = []
-        for st, (dst, src) in zip(self._copy_streams,
-                                  ((Q, hQ), (K, hK), (V, hV))):
-            st.wait_stream(main)  # the buffers are free once earlier work is done
-            with torch.cuda.stream(st):
-                dst.copy_(src, non_blocking=True)
-                if dst is Q:
-                    token_ids.copy_(htoken_ids, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(st)
-            done.append(ev)
-        main.wait_event(done[0])
-        main.wait_event(done[1])
+        if not hasattr(self, "_copy_stream"):
+            self._copy_stream = torch.cuda.Stream(self.device)
+        cs = self._copy_stream
+        cs.wait_stream(main)  # the buffers are free once earlier work is done
+        qk_ready, v_ready = torch.cuda.Event(), torch.cuda.Event()
+        with torch.cuda.stream(cs):
+            token_ids.copy_(htoken_ids, non_blocking=True)
+            Q.copy_(hQ, non_blocking=True)
+            K.copy_(hK, non_blocking=True)
+            qk_ready.record(cs)
+            V.copy_(hV, non_blocking=True)
+            v_ready.record(cs)
+        main.wait_event(qk_ready)
         self.profile(Q, K, token_ids)
-        main.wait_event(done[2])
+        main.wait_event(v_ready)
         self.compact(K, V)
 
     def decode(self, q, k_new, v_new, new_ids, pos, out=None):

@@ -271,3 +271,27 @@ def test_long32k_full_size_sampled():
     rep = compare(cfg, gpu, range(len(heads)), oracle=ora)
     print("long32k", rep)
     assert rep["decode_checked"] >= len(heads) // 2, rep
+
+
+def test_prefill_from_pinned_host_buffers_matches_device_prefill():
+    """prefill_host (copies on a copy stream, profiling overlapping the V
+    copy) builds exactly the caches that prefill builds from device tensors."""
+    from adaptive_head_kv_gb300.session import FastGenSession, make_params
+    from synth import make_workload_split, punct_ids, special_ids
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=4, n=300, steps=4)
+    w = make_workload_split(cfg, pin=True)
+    dev, n = torch.device("cuda"), cfg.n
+    p = make_params(cfg.B, cfg.L, cfg.H, n, cfg.d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f)
+    hids = torch.from_numpy(w["ids"][:, :n].copy()).pin_memory()
+    a = FastGenSession(p, special_ids(), punct_ids(), cfg.steps)
+    b = FastGenSession(p, special_ids(), punct_ids(), cfg.steps)
+    a.prefill(w["Q"].to(dev), w["K"].to(dev), w["V"].to(dev), hids.to(dev))
+    Q, K, V = (torch.empty_like(w[x], device=dev) for x in "QKV")
+    ids = torch.empty_like(hids, device=dev)
+    b.prefill_host(w["Q"], w["K"], w["V"], hids, Q, K, V, ids)
+    torch.cuda.synchronize()
+    for name in ("policy", "mass", "colsum", "keep", "kept", "pos_pool"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    live = a.pos_pool >= 0
+    assert torch.equal(a.K_pool[live], b.K_pool[live]) and torch.equal(a.V_pool[live], b.V_pool[live])
