@@ -236,7 +236,8 @@ def run_ours(args, cfg, rank, world):
     q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
     ids, dec_ids = hids.to(dev), hdec_ids.to(dev)
     p = make_params(cfg.B, cfg.L, cfg.H, n, d, cfg.dtype, cfg.T, cfg.r_l, cfg.r_f, Hkv=cfg.Hkv)
-    s = FastGenSession(p, special_ids(rank), punct_ids(rank), steps, device=dev)
+    s = FastGenSession(p, special_ids(rank), punct_ids(rank), steps, device=dev,
+                       refresh_period=args.refresh_period)
     stream = torch.cuda.current_stream()
 
     graph = None
@@ -301,6 +302,8 @@ def run_ours(args, cfg, rank, world):
     # cache + ring positions + descriptors
     dec_bytes_t = (rows_t * d * 2 * eb + G * d * eb * 2 + Gkv * d * eb * 2 + ring_t * 4
                    + Gkv * 40)
+    if args.refresh_period:  # per cached row: its score written and read, its acc updated
+        dec_bytes_t = dec_bytes_t + rows_t * 16
     dec_gbs = dec_bytes_t.sum() / (dec_ms.sum() * 1e-3) / 1e9
     prof_flops = 2.0 * n * (n + 1) * d * G
     kept_rows = int((ckeep != 0).sum())
@@ -548,6 +551,9 @@ def main():
     ap.add_argument("--T", type=float, default=None, help="override the recover ratio")
     ap.add_argument("--hkv", type=int, default=0,
                     help="key/value heads per layer (grouped-query attention); 0 = H")
+    ap.add_argument("--refresh-period", type=int, default=0,
+                    help="decode with the opt-in refresh of the frequent sets every P steps "
+                         "(fastgen_decode_attn_refresh); 0 = the frozen sets (default)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every decode call from the host instead of one CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
@@ -632,7 +638,8 @@ def main():
                    "G": cfg.G, "parallelism": f"replicas x{world}",
                    "l2": "inputs and caches larger than L2 (no flush)",
                    "step": "profile + plan + compact + all decode steps",
-                   "decode_launch": "host loop" if args.no_graph else "one CUDA graph per step"},
+                   "decode_launch": "host loop" if args.no_graph else "one CUDA graph per step",
+                   "frequent_refresh_period": args.refresh_period or None},
         "decode_tok_s": decode_tok_s, "decode_hbm_gbs": r["dec_gbs"],
         "phases_ms": {"profile": r["prof_ms"], "compact_plan": r["comp_ms"],
                       "decode_all_steps": r["decode_ms"], "decode_per_step": dec_launch_ms},
@@ -648,8 +655,11 @@ def main():
                 "decode_tok_s": world * cfg.B * cfg.steps / (e["decode_ms"] * 1e-3),
                 "decode_h2d_bytes_per_step": e["dec_h2d"],
                 "decode_d2h_bytes_per_step": e["dec_d2h"]},
-        "gpu_launches": args.steps * (fg_launches("profile") + fg_launches("plan")
-                                      + fg_launches("compact") + cfg.steps * fg_launches("decode")),
+        "gpu_launches": args.steps * (
+            fg_launches("profile") + fg_launches("plan") + fg_launches("compact")
+            + (fg_launches("refresh_init") if args.refresh_period else 0)
+            + cfg.steps * fg_launches("decode" if not args.refresh_period else "decode_acc")
+            + (cfg.steps // args.refresh_period if args.refresh_period else 0)),
     }
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg)
