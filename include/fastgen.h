@@ -383,8 +383,8 @@ fg_status fastgen_decode_attn_refresh(const fg_params* p, void* plan, const fg_p
  *     work items at d = 128 without groups, 8,000 with groups of 2, 2,000
  *     with groups of 8 (one work item covers info->rows_per_work = 256 or 512
  *     rows of one cache).  The 7B attention shape (1024 heads, 2048-token
- *     prompt, 256 new tokens: about 5,000 items) fits; the 13B, 65B and
- *     long-prompt shapes do not.  Larger plans return FG_EWORKSPACE before
+ *     prompt, 256 new tokens: about 5,000 items) fits; the 13B and 65B
+ *     shapes (tens of thousands of items) do not.  Larger plans return FG_EWORKSPACE before
  *     anything is launched; other errors as fastgen_decode_attn.
  * ------------------------------------------------------------------------ */
 #define FASTGEN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
