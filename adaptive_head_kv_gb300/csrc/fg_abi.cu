@@ -296,7 +296,7 @@ static fg_status decode_call(const fg_params* p, void* plan, const fg_plan_info*
                              const int32_t* special_ids, int32_t n_special,
                              const int32_t* punct_ids, int32_t n_punct, int32_t pos, void* out,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                             float* row_acc, float* row_sc, void* stream) {
+                             float* row_acc, float* row_sc, float* head_ml, void* stream) {
   fg_status st = check_params(p);
   if (st != FG_OK) return st;
   if ((st = check_ids(special_ids, n_special)) != FG_OK) return st;
@@ -338,6 +338,7 @@ static fg_status decode_call(const fg_params* p, void* plan, const fg_plan_info*
   a.dev_err = dev_err;
   a.row_acc = row_acc;
   a.row_sc = row_sc;
+  a.head_ml = head_ml;
   if (info->n_work == 0) {
     cudaError_t e = cudaMemsetAsync(out, 0, (size_t)pd.G * pd.d * elem_bytes(p),
                                     (cudaStream_t)stream);
@@ -355,14 +356,15 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
                               int32_t* dev_err, void* stream) {
   return decode_call(p, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new, new_ids,
                      special_ids, n_special, punct_ids, n_punct, pos, out, workspace,
-                     workspace_bytes, dev_err, nullptr, nullptr, stream);
+                     workspace_bytes, dev_err, nullptr, nullptr, nullptr, stream);
 }
 
-// Refresh state: [acc f32 x pool_rows][sc f32 x pool_rows][role u8 x pool_rows].
+// Refresh state: [acc f32 x pool_rows][sc f32 x pool_rows][role u8 x pool_rows]
+// [(M, L) f32 x 2 x G].
 size_t fastgen_refresh_state_bytes(const fg_params* p, const fg_plan_info* info) {
   if (check_params(p) != FG_OK || !info || info->pool_rows < 0) return 0;
-  const size_t rows = (size_t)info->pool_rows;
-  return 2 * align_up(rows * sizeof(float)) + align_up(rows);
+  const size_t rows = (size_t)info->pool_rows, G = (size_t)p->B * p->L * p->H;
+  return 2 * align_up(rows * sizeof(float)) + align_up(rows) + align_up(G * 2 * sizeof(float));
 }
 
 static fg_status check_refresh(const fg_params* p, const fg_plan_info* info, const void* state,
@@ -416,9 +418,10 @@ fg_status fastgen_decode_attn_refresh(const fg_params* p, void* plan, const fg_p
   float* acc = (float*)sb;
   float* sc = (float*)(sb + align_up(rows * sizeof(float)));
   const uint8_t* role = (const uint8_t*)(sb + 2 * align_up(rows * sizeof(float)));
+  float* head_ml = (float*)(sb + 2 * align_up(rows * sizeof(float)) + align_up(rows));
   st = decode_call(p, plan, info, K_pool, V_pool, pos_pool, q, k_new, v_new, new_ids,
                    special_ids, n_special, punct_ids, n_punct, pos, out, workspace,
-                   workspace_bytes, dev_err, acc, sc, stream);
+                   workspace_bytes, dev_err, acc, sc, head_ml, stream);
   if (st != FG_OK || info->n_work == 0) return st;
   if ((pos - p->n + 1) % period != 0) return FG_OK;
   const fg::ProfileDims pd = dims(p);

@@ -598,8 +598,8 @@ __global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeA
 // forms the item weights itself (a few exp2 per item, from broadcast loads)
 // and sums its dimension over the items, so each item costs one coalesced
 // row load for the whole CTA.
-// kAcc: also add each cached row's final attention weight 2^(sc - M) / L to
-// its accumulated score (one query per cache).
+// kAcc (one query per cache): also record the head's final (M, L), from
+// which acc_kernel adds each cached row's weight 2^(sc - M) / L.
 template <typename T, int D, bool kAcc = false>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, int R, int HLkv) {
   griddep_wait();
@@ -646,21 +646,40 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
     if (pl.st) a.desc[c].n_static = hd.n_static + 1;
   }
   if constexpr (kAcc) {
-    if (M != FG_NEG_INF && L > 0.f) {
-      const float inv = 1.f / L;
-      const Placement pl = place(hd, a, HLkv, c);
-      const int ns = hd.n_static + (pl.st ? 1 : 0);
-      for (int r = t; r < ns; r += D) {
-        const long long row = hd.off + r;
-        const float sv = a.row_sc[row];
-        if (sv != FG_NEG_INF) a.row_acc[row] += exp2f(sv - M) * inv;
-      }
-      for (int r = t; r < hd.w; r += D) {
-        const long long row = hd.win_off + r;
-        const float sv = a.row_sc[row];
-        if (sv != FG_NEG_INF) a.row_acc[row] += exp2f(sv - M) * inv;
-      }
+    if (t == 0) {
+      a.head_ml[2 * g] = M;
+      a.head_ml[2 * g + 1] = L;
     }
+  }
+}
+
+// Adds every cached row's weight of the step, 2^(sc - M) / L with its head's
+// final (M, L), to the row's accumulated score: one CTA per work item, one
+// thread per row (the item's rows as the split kernel saw them).
+__global__ void __launch_bounds__(kDecThreads) acc_kernel(const DecodeArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int2 it = a.work[blockIdx.x];
+  const fg_head_desc hd = a.desc[it.x];
+  const int rpw = a.rpw;
+  const int nsc = hd.n_work - cdiv(hd.w, rpw);
+  long long base;
+  int r0, r1;
+  if (it.y < nsc) {  // never-evicted segment (its row count already includes the new token)
+    base = hd.off;
+    r0 = it.y * rpw;
+    r1 = it.y == nsc - 1 ? hd.n_static : min(r0 + rpw, hd.n_static);
+  } else {
+    base = hd.win_off;
+    r0 = (it.y - nsc) * rpw;
+    r1 = min(r0 + rpw, hd.w);
+  }
+  const float M = a.head_ml[2 * it.x], L = a.head_ml[2 * it.x + 1];
+  if (M == FG_NEG_INF || !(L > 0.f)) return;
+  const float inv = 1.f / L;
+  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    const float sv = a.row_sc[base + r];
+    if (sv != FG_NEG_INF) a.row_acc[base + r] += exp2f(sv - M) * inv;
   }
 }
 
@@ -671,6 +690,7 @@ cudaError_t run_acc(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) 
                              pd.HLkv, pd.sl2);
   if (e == cudaSuccess)
     e = launch_pdl(combine_kernel<T, D, true>, pd.G, D, 0, s, a, pd.H, pd.R, pd.HLkv);
+  if (e == cudaSuccess) e = launch_pdl(acc_kernel, a.n_work, kDecThreads, 0, s, a);
   return e;
 }
 
@@ -707,7 +727,7 @@ cudaError_t run_r(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s) {
   if (a.row_acc) {
-    if (pd.R != 1 || !a.row_sc) return cudaErrorInvalidValue;
+    if (pd.R != 1 || !a.row_sc || !a.head_ml) return cudaErrorInvalidValue;
     if (pd.dtype == FG_FP32)
       return pd.d == 64 ? run_acc<float, 64>(pd, a, s) : run_acc<float, 128>(pd, a, s);
     return pd.d == 64 ? run_acc<__nv_bfloat16, 64>(pd, a, s)

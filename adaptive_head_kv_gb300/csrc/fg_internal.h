@@ -112,10 +112,12 @@ struct DecodeArgs {
   float* part_acc;  // [n_work, R, d]
   int32_t* dev_err;
   // accumulated attention of every pool row (refresh of C_frequent; no groups):
-  // when non-null the split kernel writes each row's score to row_sc and the
-  // combine adds its final weight to row_acc
+  // when non-null the split kernel writes each row's score to row_sc, the
+  // combine each head's final (M, L) to head_ml, and a third kernel adds each
+  // row's weight to row_acc
   float* row_acc = nullptr;
   float* row_sc = nullptr;
+  float* head_ml = nullptr;  // [G, 2]: each head's final (M, L) of the step
 };
 
 cudaError_t launch_decode(const ProfileDims& pd, const DecodeArgs& a, cudaStream_t s);

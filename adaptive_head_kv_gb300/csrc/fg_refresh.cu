@@ -11,10 +11,12 @@
 //        attention weight every later step's query gives it;
 //   sc   [pool_rows] f32: the current step's score of the row (base-2
 //        logit, -inf for rows not attended), written by the split kernel and
-//        turned into acc += 2^(sc - M) / L by the combine kernel;
+//        turned into acc += 2^(sc - M) / L after the combine (acc_kernel);
 //   role [pool_rows] u8: 1 for the never-evicted slots that hold frequent
 //        members, 0 otherwise.  Set once here; a refresh swaps rows between
-//        a frequent slot and the window ring, so the slots keep their role.
+//        a frequent slot and the window ring, so the slots keep their role;
+//   ml   [G, 2] f32: each head's softmax maximum and sum of the step (written
+//        by the combine kernel, read by the kernel that updates acc).
 //
 // Refresh of one local-hybrid cache (one CTA, after the step's combine):
 //   candidates = the rows in frequent slots and the rows of the window ring;

@@ -23,7 +23,7 @@ FG_KEEP_DROP, FG_KEEP_STATIC, FG_KEEP_WINDOW = 0, 1, 2
 
 # kernels launched by one call of each entry point (counted in the bench)
 LAUNCHES = {"profile": 4, "profile_attn": 5, "profile_with_policy": 5, "plan": 3, "compact": 1,
-            "decode": 2, "decode_acc": 2, "refresh": 1, "refresh_init": 1}
+            "decode": 2, "decode_acc": 3, "refresh": 1, "refresh_init": 1}
 
 EXPORTS = (
     "fastgen_status_string", "fastgen_version", "fastgen_profile_workspace_bytes",

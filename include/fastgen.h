@@ -320,7 +320,8 @@ fg_status fastgen_decode_attn(const fg_params* p, void* plan, const fg_plan_info
  * FG_EINVAL).
  *
  * fastgen_refresh_state_bytes: size of the caller-owned state (per pool
- *   row: acc float, the step's score float, a role byte), 256-byte aligned.
+ *   row: acc float, the step's score float, a role byte; per head: the step's
+ *   softmax maximum and sum), 256-byte aligned.
  * fastgen_refresh_init: after fastgen_compact, sets acc from colsum [G, n]
  *   (fastgen_profile's output) and marks the frequent slots from token_ids
  *   [B, n] and the id sets.  Asynchronous on `stream`.

@@ -217,7 +217,7 @@ def test_refresh_calls_reject_on_host():
     p = P()
     info = fg.PlanInfo(1000, 10, 256)
     st = fg.fastgen_refresh_state_bytes(p, info)
-    assert st == 2 * al(1000 * 4) + al(1000)
+    assert st == 2 * al(1000 * 4) + al(1000) + al(6 * 2 * 4)  # rows' acc, score, role; heads' (M, L)
     ws = fg.fastgen_decode_workspace_bytes(p, info)
 
     def dec(params=p, period=4, state=FAKE, state_bytes=st):
