@@ -115,9 +115,11 @@ __device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi
 // R = queries per cache (group size).  Rows are unrolled by U per warp so
 // that 2 * U 16-byte loads per thread are in flight.
 // kAcc (one query per cache): also write every row's score to a.row_sc.
+// Single-query bf16 caches keep four CTAs per SM (64 registers): the row
+// stream needs that many rows in flight.
 template <typename T, int D, int R, bool kAcc = false>
-__global__ void __launch_bounds__(kDecThreads) split_kernel(const DecodeArgs a, int H, int HLkv,
-                                                           float sl2) {
+__global__ void __launch_bounds__(kDecThreads, R == 1 && sizeof(T) == 2 ? 4 : 1)
+    split_kernel(const DecodeArgs a, int H, int HLkv, float sl2) {
   static_assert(!kAcc || R == 1, "row scores are kept for single-query caches only");
   constexpr int E = Vec16<T>::kElems;
   constexpr int LPR = D / E;     // lanes per row
