@@ -295,3 +295,35 @@ def test_prefill_from_pinned_host_buffers_matches_device_prefill():
         assert torch.equal(getattr(a, name), getattr(b, name)), name
     live = a.pos_pool >= 0
     assert torch.equal(a.K_pool[live], b.K_pool[live]) and torch.equal(a.V_pool[live], b.V_pool[live])
+
+
+def test_decode_work_list_covers_every_row_once():
+    """The plan's work list: per cache, max(1, ceil(kept static rows / rpw))
+    items for the never-evicted segment (the last also takes the appended
+    rows) and ceil(w / rpw) for the ring, listed cache by cache; small plans
+    use 256-row items."""
+    import ctypes
+
+    from adaptive_head_kv_gb300 import fastgen as fg
+
+    cfg = CONFIGS["tiny"].with_(dtype="bf16", d=128, L=2, H=6, n=700, steps=300,
+                                one_of_each=False)
+    gpu = run_gpu(cfg)
+    s = gpu["session"]
+    rpw = s.info.rows_per_work
+    assert rpw == 256
+    al = lambda x: (x + 255) // 256 * 256
+    woff = al(s.Gkv * ctypes.sizeof(fg.HeadDesc)) + al(s.Gkv * 8) + 256
+    raw = s.plan[woff: woff + s.info.n_work * 8].cpu().numpy().view(np.int32).reshape(-1, 2)
+    expect, off = [], 0
+    for c, d in enumerate(gpu["desc0"]):
+        nsc = max(1, -(-d.n_static // rpw))
+        assert d.n_work == nsc + -(-d.w // rpw), c
+        assert d.work_off == off
+        expect += [(c, i) for i in range(d.n_work)]
+        off += d.n_work
+    assert off == s.info.n_work
+    assert [tuple(x) for x in raw.tolist()] == expect
+    # full-cache heads appended 300 rows past the prompt: their last item grew
+    assert any(d.n_static > (max(1, -(-gpu["desc0"][c].n_static // rpw))) * rpw
+               for c, d in enumerate(gpu["desc1"]))
