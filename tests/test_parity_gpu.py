@@ -324,6 +324,12 @@ def test_decode_work_list_covers_every_row_once():
         off += d.n_work
     assert off == s.info.n_work
     assert [tuple(x) for x in raw.tolist()] == expect
-    # full-cache heads appended 300 rows past the prompt: their last item grew
-    assert any(d.n_static > (max(1, -(-gpu["desc0"][c].n_static // rpw))) * rpw
-               for c, d in enumerate(gpu["desc1"]))
+    # a full cache appends every generated token: its last item grew past rpw
+    # rows while the outputs still matched the oracle (compared above)
+    for c, d in enumerate(gpu["desc1"]):
+        if d.policy == fg.FG_POLICY_FULL:
+            nsc = max(1, -(-gpu["desc0"][c].n_static // rpw))
+            assert d.n_static == gpu["desc0"][c].n_static + cfg.steps
+            assert d.n_static - (nsc - 1) * rpw > rpw, c
+    rep = compare(cfg, gpu, list(range(cfg.G)))
+    assert rep["decode_checked"] >= cfg.G // 2, rep
