@@ -325,7 +325,7 @@ def test_decode_work_list_covers_every_row_once():
     assert off == s.info.n_work
     assert [tuple(x) for x in raw.tolist()] == expect
     # a full cache appends every generated token: its last item grew past rpw
-    # rows while the outputs still matched the oracle (compared above)
+    # rows, and the outputs match the oracle (compared below)
     for c, d in enumerate(gpu["desc1"]):
         if d.policy == fg.FG_POLICY_FULL:
             nsc = max(1, -(-gpu["desc0"][c].n_static // rpw))
