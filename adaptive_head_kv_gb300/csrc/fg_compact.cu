@@ -135,19 +135,26 @@ __global__ void worklist_kernel(const fg_head_desc* __restrict__ desc, int G,
   for (int i = 0; i < hd.n_work; ++i) work[hd.work_off + i] = make_int2(g, i);
 }
 
-// One CTA per (cache, chunk of kCompactChunk prompt positions): the CTA first
+// One CTA per (cache, chunk of `chunk` prompt positions): the CTA first
 // counts the never-evicted rows before its chunk (their count is the first
 // row it fills), then scans its positions in tiles of 256 and copies each
 // tile's kept rows with 16-byte vectors, one row per LPR lanes.  A window
 // position's ring slot (position mod w) is written by the CTA that owns the
 // position: its position if the row lives in the window, else the empty
 // marker; chunk 0 also marks the segment's reserve rows empty.
+// Chunk length: 512 positions, or n / 8 for long prompts, so that a cache has
+// at most eight chunks and the counting of earlier rows (linear in the
+// chunk's start) stays a small part of the work.
 constexpr int kCompactChunk = 512;
+constexpr int kMaxCompactChunks = 8;
+inline int compact_chunk(int n) {
+  return max(kCompactChunk, cdiv(cdiv(n, kMaxCompactChunks), 256) * 256);
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
     const T* __restrict__ K, const T* __restrict__ V, const uint8_t* __restrict__ keep,
-    const fg_head_desc* __restrict__ desc, int n, int H, int R, T* __restrict__ Kp,
+    const fg_head_desc* __restrict__ desc, int n, int chunk, int H, int R, T* __restrict__ Kp,
     T* __restrict__ Vp, int32_t* __restrict__ posp) {
   constexpr int E = Vec16<T>::kElems;
   constexpr int LPR = D / E;  // 16-byte vectors per row
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
   __shared__ int src_pos[kCompactThreads];
   __shared__ long long dst_row[kCompactThreads];
   const int g = blockIdx.y;  // key/value head
-  const int j0 = blockIdx.x * kCompactChunk, j1 = min(j0 + kCompactChunk, n);
+  const int j0 = blockIdx.x * chunk, j1 = min(j0 + chunk, n);
   const fg_head_desc hd = desc[g];
   const int Hkv = H / R;
   const size_t g0 = (size_t)(g / Hkv) * H + (size_t)(g % Hkv) * R;  // its first query head
@@ -207,9 +214,11 @@ template <typename T, int D>
 cudaError_t run_compact(const ProfileDims& pd, const void* K, const void* V, const uint8_t* keep,
                         const fg_head_desc* desc, void* Kp, void* Vp, int32_t* posp,
                         cudaStream_t s) {
-  const dim3 grid(cdiv(pd.n, kCompactChunk), pd.Gkv);
+  const int chunk = compact_chunk(pd.n);
+  const dim3 grid(cdiv(pd.n, chunk), pd.Gkv);
   compact_kernel<T, D><<<grid, kCompactThreads, 0, s>>>((const T*)K, (const T*)V, keep, desc,
-                                                        pd.n, pd.H, pd.R, (T*)Kp, (T*)Vp, posp);
+                                                        pd.n, chunk, pd.H, pd.R, (T*)Kp, (T*)Vp,
+                                                        posp);
   return cudaGetLastError();
 }
 
