@@ -164,6 +164,8 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
                                          float sl2, int c0, int lo, int band, float& cs,
                                          float& bs) {
   constexpr int kCols = NC * 32;
+  // every column precedes every lane's key (leading chunks of the diagonal tile)
+  if (__all_sync(0xffffffffu, lo >= c0 + kCols)) return;
   const uint64_t s2 = pack2(sl2, sl2);
   // no lane of the warp needs a per-element test: one packed path
   if (__all_sync(0xffffffffu, lo <= c0 && (band <= c0 || band >= c0 + kCols))) {
@@ -194,28 +196,32 @@ __device__ __forceinline__ void col_tile(const uint32_t (&r)[NC][32], const floa
   // band edge falls in these columns).  The decision is made for the whole
   // warp, so its lanes never split between two paths: every lane runs the
   // packed arithmetic, the causal test only when some lane needs it, and the
-  // band split by a per-element select.
+  // band split by 0/1 weights, each the saturated difference of two exact
+  // small integers (the lane's band end and the column offset).
   const bool diag = __any_sync(0xffffffffu, lo > c0);
+  const float dband = (float)(band - c0);
   uint64_t at = 0, ab = 0;
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const int col = c0 + c * 32 + e;
+      const float k = (float)(c * 32 + e);
       const float4 L = Lv[c * 8 + e / 4];
       float x0, x1, x2, x3;
       unpack2(fma2(pack2(f(r[c][e]), f(r[c][e + 1])), s2, pack2(L.x, L.y)), x0, x1);
       unpack2(fma2(pack2(f(r[c][e + 2]), f(r[c][e + 3])), s2, pack2(L.z, L.w)), x2, x3);
-      float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-      if (diag) {
-        p0 = col < lo ? 0.f : p0;
-        p1 = col + 1 < lo ? 0.f : p1;
-        p2 = col + 2 < lo ? 0.f : p2;
-        p3 = col + 3 < lo ? 0.f : p3;
+      uint64_t p01 = pack2(ex2(x0), ex2(x1)), p23 = pack2(ex2(x2), ex2(x3));
+      if (diag) {  // a select, not a product: a score past the key may overflow
+        const int col = c0 + c * 32 + e;
+        float p0, p1, p2, p3;
+        unpack2(p01, p0, p1);
+        unpack2(p23, p2, p3);
+        p01 = pack2(col < lo ? 0.f : p0, col + 1 < lo ? 0.f : p1);
+        p23 = pack2(col + 2 < lo ? 0.f : p2, col + 3 < lo ? 0.f : p3);
       }
-      at = add2(at, add2(pack2(p0, p1), pack2(p2, p3)));
-      ab = add2(ab, add2(pack2(col < band ? p0 : 0.f, col + 1 < band ? p1 : 0.f),
-                         pack2(col + 2 < band ? p2 : 0.f, col + 3 < band ? p3 : 0.f)));
+      at = add2(at, add2(p01, p23));
+      ab = fma2(p01, pack2(__saturatef(dband - k), __saturatef(dband - k - 1.f)), ab);
+      ab = fma2(p23, pack2(__saturatef(dband - k - 2.f), __saturatef(dband - k - 3.f)), ab);
     }
   float t0, t1, b0, b1;
   unpack2(at, t0, t1);
