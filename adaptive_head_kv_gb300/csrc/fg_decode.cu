@@ -35,19 +35,41 @@ constexpr int kDecWarps = kDecThreads / 32;
 struct Placement {
   bool st;        // joins the never-evicted segment
   bool overflow;  // wanted to, but the segment is full
-  bool ring_put;  // goes into the window ring
+};
+
+// The parts of a work item fixed before the step: the item, its cache's
+// descriptor and the step token's class.  Kernels read them before waiting
+// on the previous kernel (programmatic launch), which never writes them: the
+// plan wrote the work list and descriptors, the caller the token ids.  Only
+// the segment's row count (n_static) changes from step to step (the combine
+// advances it); it is read after the wait, from L2, since the descriptor's
+// line may sit in L1 from the earlier read.
+struct ItemStatic {
+  int2 it;          // (cache, item of the cache)
+  fg_head_desc hd;  // its n_static is not current until live_rows replaces it
+  bool is_s, is_p;  // the step's token is special / punctuation
 };
 
 // c: cache (key/value head) index; HLkv = L * Hkv caches per sequence.
-__device__ __forceinline__ Placement place(const fg_head_desc& hd, const DecodeArgs& a, int HLkv,
-                                           int c) {
-  const int tau = a.new_ids[c / HLkv];
-  const bool is_s = id_in(tau, a.special, a.ns), is_p = id_in(tau, a.punct, a.np);
+__device__ __forceinline__ ItemStatic item_static(const DecodeArgs& a, int HLkv, int2 it) {
+  ItemStatic s;
+  s.it = it;
+  s.hd = a.desc[it.x];
+  const int tau = a.new_ids[it.x / HLkv];
+  s.is_s = id_in(tau, a.special, a.ns);
+  s.is_p = id_in(tau, a.punct, a.np);
+  return s;
+}
+
+__device__ __forceinline__ int live_rows(const DecodeArgs& a, int c) {
+  return __ldcg(&a.desc[c].n_static);
+}
+
+__device__ __forceinline__ Placement place(const fg_head_desc& hd, bool is_s, bool is_p) {
   Placement pl;
   pl.st = joins_static(hd.policy, is_s, is_p);
   pl.overflow = pl.st && hd.n_static >= hd.static_cap;
   if (pl.overflow) pl.st = false;
-  pl.ring_put = hd.policy == FG_POLICY_SPFL && !pl.st && !pl.overflow && hd.w > 0;
   return pl;
 }
 
@@ -61,36 +83,48 @@ struct Item {
   long long base;  // first pool row of the segment
 };
 
-// Reads work item wi, writes the new token's row if its slot falls in the item
-// (the only writer of that row) and marks an evicted ring row empty.
+// Sets up work item s.it (after the wait), writes the new token's row if its
+// slot falls in the item (the only writer of that row) and marks an evicted
+// ring row empty.  Only the segment's last item depends on the live row
+// count: every earlier item was full at the prompt's end (the plan gives a
+// segment ceil(kept / rpw) items) and never holds the new slot, and whether
+// the token enters the ring does not depend on the count either (it does
+// unless it is one the never-evicted segment takes, whether or not that
+// segment has room).
 template <typename T, int D>
-__device__ __forceinline__ Item item_setup(const DecodeArgs& a, int HLkv, int wi) {
+__device__ __forceinline__ Item item_setup(const DecodeArgs& a, const ItemStatic& s) {
   constexpr int LPR = D / Vec16<T>::kElems;
-  const int2 it = a.work[wi];
   Item m;
-  m.c = it.x;
-  int chunk = it.y;
-  const fg_head_desc hd = a.desc[m.c];
-  const Placement pl = place(hd, a, HLkv, m.c);
+  m.c = s.it.x;
+  int chunk = s.it.y;
+  fg_head_desc hd = s.hd;
   const int rpw = a.rpw;
   const int nsc = hd.n_work - cdiv(hd.w, rpw);  // items of the never-evicted segment
   m.ring = chunk >= nsc;
   m.evict = -1;
+  m.new_slot = -1;
   if (!m.ring) {
-    const int rows = hd.n_static + (pl.st ? 1 : 0);
     m.r0 = chunk * rpw;
-    m.r1 = chunk == nsc - 1 ? rows : min(m.r0 + rpw, rows);
     m.base = hd.off;
-    m.new_slot = pl.st ? hd.n_static : -1;
-    if (pl.overflow && chunk == 0 && threadIdx.x == 0) atomicOr(a.dev_err, 1);
+    if (chunk == nsc - 1) {
+      hd.n_static = live_rows(a, m.c);
+      const Placement pl = place(hd, s.is_s, s.is_p);
+      m.r1 = hd.n_static + (pl.st ? 1 : 0);
+      m.new_slot = pl.st ? hd.n_static : -1;
+      if (pl.overflow && threadIdx.x == 0) atomicOr(a.dev_err, 1);
+    } else {
+      m.r1 = m.r0 + rpw;
+    }
   } else {
     chunk -= nsc;
     m.r0 = chunk * rpw;
     m.r1 = min(m.r0 + rpw, hd.w);
     m.base = hd.win_off;
     const int slot = a.pos % hd.w;
-    m.new_slot = pl.ring_put ? slot : -1;
-    m.evict = pl.ring_put ? -1 : slot;  // the row that left the window
+    const bool ring_put = hd.policy == FG_POLICY_SPFL && hd.w > 0 &&
+                          !joins_static(hd.policy, s.is_s, s.is_p);
+    m.new_slot = ring_put ? slot : -1;
+    m.evict = ring_put ? -1 : slot;  // the row that left the window
   }
   if (m.new_slot >= m.r0 && m.new_slot < m.r1) {
     T* Kp = (T*)a.Kp;
@@ -131,10 +165,11 @@ __global__ void __launch_bounds__(kDecThreads, R == 1 && sizeof(T) == 2 ? 4 : 1)
   __shared__ float sm_m[R][kDecWarps], sm_l[R][kDecWarps];
   __shared__ float sm_acc[R][kDecWarps][D];
 
+  const ItemStatic st = item_static(a, HLkv, a.work[blockIdx.x]);
   griddep_wait();
   griddep_launch_dependents();
+  const Item it = item_setup<T, D>(a, st);
   const int wi = blockIdx.x;
-  const Item it = item_setup<T, D>(a, HLkv, wi);
   const int c = it.c, r0 = it.r0, r1 = it.r1, new_slot = it.new_slot, evict = it.evict;
   const bool ring = it.ring;
   const long long base = it.base;
@@ -404,10 +439,11 @@ __global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeA
   extern __shared__ __align__(16) uint8_t mma_smem[];
   __shared__ float sm_m[kMmaWarps][R], sm_l[kMmaWarps][R], sm_f[kMmaWarps][R];
 
+  const ItemStatic st = item_static(a, HLkv, a.work[blockIdx.x]);
   griddep_wait();
   griddep_launch_dependents();
+  const Item it = item_setup<T, D>(a, st);
   const int wi = blockIdx.x;
-  const Item it = item_setup<T, D>(a, HLkv, wi);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const T* Kp = (const T*)a.Kp;
@@ -604,12 +640,17 @@ __global__ void __launch_bounds__(kMmaThreads, 4) split_mma_kernel(const DecodeA
 // which acc_kernel adds each cached row's weight 2^(sc - M) / L.
 template <typename T, int D, bool kAcc = false>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, int R, int HLkv) {
-  griddep_wait();
-  griddep_launch_dependents();
   const int g = blockIdx.x;  // query head
   const int t = threadIdx.x;
   const int c = kv_head(g, H, R), q = (g % H) % R;  // its cache and place in the group
-  const fg_head_desc hd = a.desc[c];
+  ItemStatic st = item_static(a, HLkv, make_int2(c, 0));
+  griddep_wait();
+  griddep_launch_dependents();
+  const fg_head_desc& hd = st.hd;
+  // one member advances the shared cache; its row count is requested now so
+  // that the load overlaps the partials'
+  const bool bump = t == 0 && q == 0;
+  const int live = bump ? live_rows(a, c) : 0;
   const size_t w0 = (size_t)hd.work_off;
   const int nw = hd.n_work;
   // items in chunks of 8: every load of a chunk is issued before any is used
@@ -643,9 +684,10 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
     M = Mn;
   }
   store_out((T*)a.out + (size_t)g * D + t, L > 0.f ? acc / L : 0.f);
-  if (t == 0 && q == 0) {  // one member advances the shared cache
-    const Placement pl = place(hd, a, HLkv, c);
-    if (pl.st) a.desc[c].n_static = hd.n_static + 1;
+  if (bump) {
+    st.hd.n_static = live;
+    const Placement pl = place(st.hd, st.is_s, st.is_p);
+    if (pl.st) a.desc[c].n_static = live + 1;
   }
   if constexpr (kAcc) {
     if (t == 0) {
@@ -659,10 +701,11 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a, int H, i
 // final (M, L), to the row's accumulated score: one CTA per work item, one
 // thread per row (the item's rows as the split kernel saw them).
 __global__ void __launch_bounds__(kDecThreads) acc_kernel(const DecodeArgs a) {
+  const int2 it = a.work[blockIdx.x];
+  fg_head_desc hd = a.desc[it.x];
   griddep_wait();
   griddep_launch_dependents();
-  const int2 it = a.work[blockIdx.x];
-  const fg_head_desc hd = a.desc[it.x];
+  hd.n_static = live_rows(a, it.x);
   const int rpw = a.rpw;
   const int nsc = hd.n_work - cdiv(hd.w, rpw);
   long long base;

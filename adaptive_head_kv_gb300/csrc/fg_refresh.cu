@@ -98,8 +98,11 @@ __global__ void __launch_bounds__(kRefreshThreads) refresh_kernel(
   __shared__ int s_cnt, s_kf;
   griddep_wait();
   griddep_launch_dependents();
-  const fg_head_desc hd = desc[blockIdx.x];
+  fg_head_desc hd = desc[blockIdx.x];
   if (hd.policy != FG_POLICY_SPFL || hd.w <= 0) return;  // no window: nothing to promote
+  // the row count that the step's combine advanced, read from L2: decode
+  // kernels read descriptors before their wait, so a line in L1 may be older
+  hd.n_static = __ldcg(&desc[blockIdx.x].n_static);
   if (threadIdx.x == 0) {
     s_cnt = 0;
     s_kf = 0;
