@@ -1,5 +1,9 @@
 """Host-side bookkeeping of bench.py: the per-step cache sizes used for the
-decode roofline equal the oracle's cache sets."""
+decode roofline equal the oracle's cache sets, the CPU baseline's sample is
+bounded, and the DRAM traffic figures are scaled, merged and voided as
+their sources change."""
+import json
+
 import numpy as np
 
 import bench
@@ -50,3 +54,58 @@ def test_cpu_baseline_sample_is_bounded_and_reported():
     assert rep["sample"].startswith("1 of 4 heads")
     full = bench.cpu_baseline(cfg, max_heads=3, budget_s=None)
     assert full["sample"].startswith("3 of 4 heads")
+
+
+def _ncu_csv(path, launches):
+    """An ncu --csv log in the layout the profiler writes: notes, a header,
+    then one row per (launch, metric)."""
+    cols = ["ID", "Process ID", "Process Name", "Host Name", "Kernel Name", "Context", "Stream",
+            "Block Size", "Grid Size", "Device", "CC", "Section Name", "Metric Name",
+            "Metric Unit", "Metric Value"]
+    lines = ["==PROF== Connected to process 1", ",".join(f'"{c}"' for c in cols)]
+    for i, (kernel, metrics) in enumerate(launches):
+        for name, unit, value in metrics:
+            row = [str(i), "1", "python3", "host", kernel, "1", "7", "(256, 1, 1)", "(8, 1, 1)",
+                   "0", "10.3", "Command line profiler metrics", name, unit, value]
+            lines.append(",".join(f'"{c}"' for c in row))
+    path.write_text("\n".join(lines) + "\n")
+
+
+def test_traffic_record_scales_merges_and_expires(tmp_path, monkeypatch):
+    """record_traffic: DRAM bytes per call of a kernel group (read + write of
+    every kernel of the group, divided by the launches of the group's
+    call-counting kernel), scaled to the full workload when captured on a
+    smaller case, merged with the other groups already recorded; load_traffic
+    returns the figure only for the same workload and unchanged sources."""
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "traffic.json"))
+    split = "void unnamed>::split_kernel<__nv_bfloat16, 128, 1, 0>(DecodeArgs, int, int, float)"
+    comb = "void unnamed>::combine_kernel<__nv_bfloat16, 128, 0>(DecodeArgs, int, int, int)"
+    dram = lambda r, w, u="Mbyte": [("gpu__time_duration.sum", "us", "100"),
+                                    ("dram__bytes_read.sum", u, r), ("dram__bytes_write.sum", u, w)]
+    csv_path = tmp_path / "decode.csv"
+    _ncu_csv(csv_path, [(split, dram("600", "4")), (comb, dram("2", "0.5")),
+                        (split, dram("0.61", "0.003", "Gbyte")), (comb, dram("2,000", "500", "Kbyte"))])
+    bench.record_traffic(str(csv_path), "llama65b", "cmd", scale={"decode": 10.0},
+                         measured_on="llama65b_L2")
+    want = ((600 + 4 + 2 + 0.5) * 1e6 + (0.61 + 0.003) * 1e9 + 2.5e6) / 2 * 10.0
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    assert set(rec) == {"decode"}
+    assert rec["decode"]["calls"] == 2 and rec["decode"]["scale"] == 10.0
+    assert abs(rec["decode"]["bytes_per_call"] - want) < 1e-3 * want
+    assert abs(bench.load_traffic("decode", "llama65b") - want) < 1e-3 * want
+    assert bench.load_traffic("decode", "llama7b") is None  # another workload
+    # a capture of another group keeps the decode figure
+    sel = "void unnamed>::select_kernel(const float *, int)"
+    prof = "void unnamed>::profile_tc_kernel<1, 128>(CUtensorMap_st, CUtensorMap_st, float *)"
+    csv2 = tmp_path / "profile.csv"
+    _ncu_csv(csv2, [(prof, dram("1000", "10")), (sel, dram("16", "0"))])
+    bench.record_traffic(str(csv2), "llama65b", "cmd2", scale={"profile": 40.0},
+                         measured_on="llama65b_L2")
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    assert set(rec) == {"decode", "profile"}
+    assert abs(rec["profile"]["bytes_per_call"] - 1026e6 * 40) < 1.0
+    # a change to a group's sources voids its figure, not the other group's
+    real = bench.source_digest
+    monkeypatch.setattr(bench, "source_digest", lambda g: "changed" if g == "profile" else real(g))
+    assert bench.load_traffic("profile", "llama65b") is None
+    assert bench.load_traffic("decode", "llama65b") is not None
